@@ -1,0 +1,497 @@
+#!/usr/bin/env python
+"""Benchmark of one CSA decode layer step on GB300.
+
+A step is one pass of the whole hot path over one batch of query tokens:
+lightning-indexer logits -> top-k -> sink-merged attention over the selected
+entries and the SWA window (the gather is fused into the attention kernel).
+The default workload is 32 sequences at 128K context (32768 compressed
+entries each), top-k 2048, SWA 128.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   (the CPU oracle on a bounded sample)
+
+Prints one JSON line (rank 0). With N > 1 (torchrun), every rank runs an
+independent replica on its own GPU (the path has no exchange step): weak
+scaling, value = tokens of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes as C
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA decode tokens/s at 128K ctx; achieved HBM GB/s and % of roofline"
+UNIT = "tokens/s"
+SCALE = 1.0 / math.sqrt(512)
+N_COPIES = 3  # rotating input copies: each step's inputs are not L2-resident
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.samples: list[tuple[float, list[str]]] = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        mine = [(t, p) for t, p in self.samples if not self.uuid or self.uuid in p[0]]
+        inside = [(t, p) for t, p in mine if t0 - 0.05 <= t <= t1 + 0.05]
+        window = "timed region"
+        if not inside and mine:  # region shorter than the sampling period: nearest samples
+            mine.sort(key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))
+            inside = mine[:3]
+            window = "nearest samples to a timed region shorter than the sampling period"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for _, p in inside if num(p[1]) is not None]
+        reasons = set()
+        for _, p in inside:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), p[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(inside[0][1][2]),
+                "power_w_max": max((num(p[3]) or 0.0) for _, p in inside), "reasons": sorted(reasons),
+                "samples": len(inside), "window": window}
+
+
+# --------------------------------------------------------------------------
+# algorithmic bytes (the roofline's numerator)
+# --------------------------------------------------------------------------
+
+def indexer_bytes(x) -> int:
+    """Bytes the indexer must move per launch: each key visible to any token
+    of its sequence (128 B codes + 4 B scale, read once for all T tokens),
+    each token's indexer query (64x128 B codes + 64 fp32 scales + 64 fp32
+    weights + position), and the fp32 logits row written in full."""
+    import numpy as np
+    wl = x.wl
+    q_pos = x.q_pos.cpu().numpy()
+    n_comp = x.n_comp.cpu().numpy()
+    nv = np.minimum(np.minimum(q_pos // wl.m, n_comp[:, None]), wl.ncap).max(axis=1)
+    keys = int(nv.sum()) * (128 + 4)
+    per_tok = 64 * 128 + 64 * 4 + 64 * 4 + 4
+    return keys + wl.B * wl.T * (per_tok + 4 * wl.ncap)
+
+
+def attention_bytes(cnt, x) -> int:
+    """Bytes the attention must move: 592 B per candidate record per query
+    (top-k entries + SWA window), the BF16 query and output rows (128 KB
+    each) and the fp32 LSE."""
+    import numpy as np
+    q_pos = x.q_pos.cpu().numpy().reshape(-1)
+    nswa = np.minimum(q_pos + 1, x.wl.W)
+    cands = int(cnt.sum()) + int(nswa.sum())
+    return cands * 592 + x.wl.B * x.wl.T * (2 * 128 * 512 * 2 + 128 * 4)
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+
+class Runner:
+    """Pre-marshalled C-ABI calls for one input copy (pointers computed once,
+    so the timed loop spends its host time in the library, not in Python)."""
+
+    def __init__(self, csd, x, stream):
+        import torch
+        self.csd, self.x, self.lib = csd, x, csd.load()
+        wl = x.wl
+        B, T, N, k = wl.B, wl.T, wl.ncap, wl.k
+        dev = x.q.device
+        self.logits = torch.empty((B, T, N), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((B, T, k), dtype=torch.int32, device=dev)
+        self.cnt = torch.empty((B, T), dtype=torch.int32, device=dev)
+        self.out = torch.empty((B, T, 128, 512), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((B, T, 128), dtype=torch.float32, device=dev)
+        self.ws_topk = csd.workspace(csd.OP_TOPK, B, T, N, k, dev)
+        self.ws_att = csd.workspace(csd.OP_ATTENTION, B, T, N, k, dev)
+        self.ws_step = csd.workspace(csd.OP_DECODE_STEP, B, T, N, k, dev)
+        self.comp = csd.cache_desc(x.comp, N, x.seq_stride, x.block_table,
+                                   x.page_records if x.block_table is not None else 0)
+        s = C.c_void_p(stream.cuda_stream)
+        p = lambda t: C.c_void_p(t.data_ptr()) if t is not None else None
+        nb = lambda t: C.c_size_t(0 if t is None else t.numel())
+        R = x.ring.shape[1]
+        self.a_idx = [p(x.q_idx), p(x.q_idx_scale), p(x.w_idx), p(x.k_idx), p(x.k_idx_scale), p(x.q_pos),
+                      p(x.n_comp), B, T, N, wl.m, p(self.logits), s]
+        self.a_topk = [p(self.logits), p(x.q_pos), p(x.n_comp), B, T, N, wl.m, k, p(self.idx), p(self.cnt),
+                       p(self.ws_topk), nb(self.ws_topk), s]
+        self.a_att = [p(x.q), p(x.sink), C.c_float(SCALE), self.comp, p(x.ring), R, wl.W, p(self.idx), p(self.cnt),
+                      p(x.q_pos), B, T, k, p(self.out), p(self.lse), p(self.ws_att), nb(self.ws_att), s]
+        self.a_step = [p(x.q_idx), p(x.q_idx_scale), p(x.w_idx), p(x.k_idx), p(x.k_idx_scale), p(x.q), p(x.sink),
+                       C.c_float(SCALE), self.comp, p(x.ring), R, wl.W, p(x.q_pos), p(x.n_comp), B, T, N, wl.m, k,
+                       p(self.out), p(self.lse), None, None, p(self.ws_step), nb(self.ws_step), s]
+
+    def indexer(self):
+        st = self.lib.csa_indexer_logits(*self.a_idx)
+        if st:
+            raise RuntimeError(f"csa_indexer_logits: {self.csd.status_string(st)}")
+
+    def topk(self):
+        st = self.lib.csa_topk(*self.a_topk)
+        if st:
+            raise RuntimeError(f"csa_topk: {self.csd.status_string(st)}")
+
+    def attention(self):
+        st = self.lib.csa_sink_attention_decode(*self.a_att)
+        if st:
+            raise RuntimeError(f"csa_sink_attention_decode: {self.csd.status_string(st)}")
+
+    def decode_step(self):
+        st = self.lib.csa_decode_step(*self.a_step)
+        if st:
+            raise RuntimeError(f"csa_decode_step: {self.csd.status_string(st)}")
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import compressed_sparse_decode_gb300 as csd
+    import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    csd.build()
+    csd.load()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    name = args.workload or synth.HEADLINE
+    base = synth.generate(name, seed=0, device=dev)
+    wl = base.wl
+    if wl.kind != "csa":
+        raise SystemExit("the decode-step benchmark runs a CSA workload")
+    copies = [base] + [base.clone() for _ in range(N_COPIES - 1)]
+    stream = torch.cuda.Stream(device=dev)
+    runners = [Runner(csd, x, stream) for x in copies]
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # warm-up: at least W steps and about half a second of continuous work
+    with torch.cuda.stream(stream):
+        t_end = time.time() + 0.5
+        i = 0
+        while i < args.warmup or time.time() < t_end:
+            r = runners[i % N_COPIES]
+            r.indexer(); r.topk(); r.attention()
+            i += 1
+            if i % 20 == 0:
+                stream.synchronize()
+    stream.synchronize()
+    if csd.csa_read_device_error(stream):
+        raise RuntimeError("device error word set during warm-up")
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # keep the GPU busy right up to the timed region (clock samples stay meaningful)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            r = runners[i % N_COPIES]
+            r.indexer(); r.topk(); r.attention()
+    barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = csd.csa_kernel_launches()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(args.steps):
+            r = runners[i % N_COPIES]
+            e0, e1, e2, e3 = ev[i]
+            e0.record(stream)
+            r.indexer()
+            e1.record(stream)
+            r.topk()
+            e2.record(stream)
+            r.attention()
+            e3.record(stream)
+        end.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    barrier()
+    launches = csd.csa_kernel_launches() - launches0
+    time.sleep(0.1)
+    clocks.stop()
+    total_ms = start.elapsed_time(end)
+    t_idx = [a.elapsed_time(b) for a, b, _, _ in ev]
+    t_topk = [b.elapsed_time(c) for _, b, c, _ in ev]
+    t_att = [c.elapsed_time(d) for _, _, c, d in ev]
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    if csd.csa_read_device_error(stream):
+        raise RuntimeError("device error word set during the timed region")
+
+    tokens = wl.B * wl.T * args.steps * world
+    value = tokens / (total_ms / 1e3)
+    peaks = load_peaks()
+    idx_bytes = indexer_bytes(base)
+    att_bytes = attention_bytes(runners[0].cnt.cpu().numpy(), base)
+    idx_ms = statistics.mean(t_idx)
+    achieved = idx_bytes / (idx_ms / 1e3) / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "indexer_traffic.json")
+    if os.path.exists(prof):
+        d = json.load(open(prof))
+        if d.get("workload") == name and d.get("kernel_source_hash") == kernel_hash():
+            traffic = d.get("dram_bytes_per_launch")
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3xe4m3->f32 indexer; f32 attention",
+        "data": "synthetic (seeded N(0,1) latents/queries, FP8 E4M3 per-block scales; no weights needed)",
+        "config": {"workload": name, "batch": wl.B, "tokens_per_seq": wl.T, "context_tokens": wl.ctx,
+                   "compressed_entries": wl.ncap, "m": wl.m, "topk": wl.k, "swa": wl.W,
+                   "l2": f"inputs larger than L2: {N_COPIES} rotating copies, each step reads a different one",
+                   "parallelism": f"replicas x{world}"},
+        "kernel_ms": {"indexer": round(idx_ms, 5), "topk": round(statistics.mean(t_topk), 5),
+                      "attention": round(statistics.mean(t_att), 5)},
+        "roofline": {"kernel": "csa_indexer_logits", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "peak_source": peaks["source"], "traffic": traffic, "algorithmic_bytes": idx_bytes},
+        "attention_roofline": {"achieved": round(att_bytes / (statistics.mean(t_att) / 1e3) / 1e9, 1),
+                               "unit": "GB/s", "algorithmic_bytes": att_bytes},
+        "gpu_launches": launches,
+        "clocks": clocks.summary(t0, t1),
+    }
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(args, csd, copies, runners, stream, dev, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(base)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(args, csd, copies, runners, stream, dev, world):
+    """Same metric through the public decode-step call with host buffers:
+    each step copies its query-side inputs from pinned host memory, runs
+    csa_decode_step, and reads the output and LSE back to pinned host memory.
+    The caches (compressed entries, indexer keys, SWA ring) are the layer's
+    device-resident state, as in decode."""
+    import torch
+    host_in = []
+    for x in copies:
+        host_in.append([t.cpu().pin_memory() for t in (x.q, x.q_idx, x.q_idx_scale, x.w_idx, x.q_pos)])
+    host_out = [(torch.empty_like(r.out, device="cpu").pin_memory(), torch.empty_like(r.lse, device="cpu").pin_memory())
+                for r in runners]
+    bi = sum(t.numel() * t.element_size() for t in host_in[0])
+    bo = sum(t.numel() * t.element_size() for t in host_out[0])
+
+    def one(i):
+        x, r = copies[i % N_COPIES], runners[i % N_COPIES]
+        for dst, src in zip((x.q, x.q_idx, x.q_idx_scale, x.w_idx, x.q_pos), host_in[i % N_COPIES]):
+            dst.copy_(src, non_blocking=True)
+        r.decode_step()
+        ho, hl = host_out[i % N_COPIES]
+        ho.copy_(r.out, non_blocking=True)
+        hl.copy_(r.lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            one(i)
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(args.steps):
+            one(i)
+        end.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = start.elapsed_time(end)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    wl = copies[0].wl
+    return {"value": round(wl.B * wl.T * args.steps * world / (ms / 1e3), 1), "unit": UNIT,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(ms / args.steps, 5),
+            "call": "csa_decode_step"}
+
+
+def kernel_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("indexer.cu", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "compressed_sparse_decode_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# --------------------------------------------------------------------------
+# the oracle (CPU baseline and reference arm)
+# --------------------------------------------------------------------------
+
+def _oracle_host_inputs(x):
+    import oracle
+    import torch
+    h = {"q_idx": x.q_idx.cpu(), "q_idx_scale": x.q_idx_scale.cpu(), "w_idx": x.w_idx.cpu(), "k_idx": x.k_idx.cpu(),
+         "k_idx_scale": x.k_idx_scale.cpu(), "q_pos": x.q_pos.cpu(), "n_comp": x.n_comp.cpu(),
+         "q": x.q.view(torch.int16).cpu(), "sink": x.sink.cpu(), "ring": x.ring.cpu().numpy()}
+    h["cache"] = oracle.Cache(x.comp.cpu().numpy(), seq_stride=x.seq_stride, seq_capacity=x.wl.ncap)
+    return h
+
+
+def _oracle_rows(h, wl, rows, threads):
+    """The oracle's full step (indexer -> top-k -> attention) on query rows."""
+    import numpy as np
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+
+    def one(r):
+        lg = oracle.indexer_logits(h["q_idx"], h["q_idx_scale"], h["w_idx"], h["k_idx"], h["k_idx_scale"], h["q_pos"],
+                                   h["n_comp"], wl.m, rows=[r])
+        b = r // wl.T
+        sl = lg.reshape(-1, wl.ncap)[r][None, None]
+        idx, cnt = oracle.topk(sl, h["q_pos"].numpy().reshape(-1)[r:r + 1][None], h["n_comp"].numpy()[b:b + 1],
+                               wl.m, wl.k)
+        full_idx = np.full((wl.B * wl.T, wl.k), -1, np.int32)
+        full_cnt = np.zeros((wl.B * wl.T,), np.int32)
+        full_idx[r], full_cnt[r] = idx[0, 0], cnt[0, 0]
+        oracle.csa_attention(h["q"], h["sink"], SCALE, h["cache"], h["ring"], wl.W,
+                             full_idx.reshape(wl.B, wl.T, wl.k), full_cnt.reshape(wl.B, wl.T), h["q_pos"], rows=[r])
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, rows))
+
+
+def cpu_baseline(x) -> dict:
+    cores = os.cpu_count() or 1
+    wl = x.wl
+    h = _oracle_host_inputs(x)
+    n = min(wl.B * wl.T, 8)
+    rows = list(range(n))
+    t0 = time.time()
+    _oracle_rows(h, wl, rows, min(cores, n))
+    dt = time.time() - t0
+    return {"value": round(n / dt, 3), "unit": UNIT, "cores": min(cores, n), "kind": "oracle",
+            "sample": f"{n} of the {wl.B * wl.T} query tokens of one decode step (indexer, top-k, attention), "
+                      f"{dt:.1f} s wall"}
+
+
+def run_reference(args, rank, world, local_rank):
+    if rank != 0:
+        return
+    import torch
+    import synth
+    name = args.workload or synth.HEADLINE
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x = synth.generate(name, seed=0, device=dev)
+    wl = x.wl
+    h = _oracle_host_inputs(x)
+    cores = os.cpu_count() or 1
+    per_step = max(1, min(wl.B * wl.T, cores))
+    rows_all = list(range(wl.B * wl.T))
+    for i in range(args.warmup):
+        _oracle_rows(h, wl, [rows_all[(i * per_step + j) % len(rows_all)] for j in range(per_step)], per_step)
+    t0 = time.time()
+    for i in range(args.steps):
+        _oracle_rows(h, wl, [rows_all[(i * per_step + j) % len(rows_all)] for j in range(per_step)], per_step)
+    dt = time.time() - t0
+    value = per_step * args.steps / dt
+    line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": name, "batch": wl.B, "tokens_per_seq": wl.T, "context_tokens": wl.ctx,
+                       "compressed_entries": wl.ncap, "m": wl.m, "topk": wl.k, "swa": wl.W},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": per_step, "kind": "oracle",
+                             "sample": f"each step: {per_step} of the {wl.B * wl.T} query tokens of the workload"},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world, local_rank)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

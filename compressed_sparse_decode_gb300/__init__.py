@@ -1,0 +1,294 @@
+"""Python binding of libcsa, the GB300 (sm_103a) CSA decode library.
+
+Argument marshalling only: every function below checks tensor devices,
+dtypes and shapes, passes raw device pointers and the current CUDA stream to
+the extern "C" entry point of the same name (include/csa.h), and raises
+``CsaError`` on a non-zero status. All compute runs in the library's CUDA
+kernels. There is no fallback: if libcsa.so is missing or cannot be loaded,
+``load()`` raises.
+
+PyTorch supplies device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import torch
+
+from ._build import LIB, build  # noqa: F401  (build() compiles libcsa.so in-tree)
+
+HEADS, DIM, NOPE, ROPE, SCALE_BLOCK, RECORD_BYTES = 128, 512, 448, 64, 128, 592
+IDX_HEADS, IDX_DIM = 64, 128
+MAX_TOKENS_PER_SEQ, MAX_TOPK, MAX_SWA_WINDOW = 4, 2048, 512
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_BAD_INDEX = range(7)
+OP_INDEXER, OP_TOPK, OP_ATTENTION, OP_HCA_ATTENTION, OP_DECODE_STEP = range(5)
+
+EXPORTED = ["csa_workspace_bytes", "csa_indexer_logits", "csa_topk", "csa_gather_swa",
+            "csa_sink_attention_decode", "hca_sink_attention_decode", "csa_decode_step",
+            "csa_read_device_error", "csa_status_string", "csa_version", "csa_kernel_launches"]
+
+
+class CsaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: status {status} ({status_string(status)})")
+        self.status = status
+
+
+class csa_cache_desc(C.Structure):
+    _fields_ = [("base", C.c_void_p), ("n_records", C.c_int64), ("seq_stride", C.c_int64),
+                ("block_table", C.c_void_p), ("page_records", C.c_int32), ("max_pages", C.c_int32),
+                ("seq_capacity", C.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: str | None = None):
+    """Load libcsa.so (built in-tree by ``build()``); raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libcsa.so not found at {path}: run compressed_sparse_decode_gb300.build()")
+        lib = C.CDLL(path)
+        P, i32, sz, f32 = C.c_void_p, C.c_int, C.c_size_t, C.c_float
+        st = C.c_int
+        lib.csa_version.restype = C.c_int
+        lib.csa_kernel_launches.restype = C.c_uint64
+        lib.csa_status_string.argtypes = [C.c_int]
+        lib.csa_status_string.restype = C.c_char_p
+        lib.csa_workspace_bytes.argtypes = [C.c_int, i32, i32, i32, i32]
+        lib.csa_workspace_bytes.restype = sz
+        lib.csa_indexer_logits.argtypes = [P] * 7 + [i32] * 4 + [P, P]
+        lib.csa_indexer_logits.restype = st
+        lib.csa_topk.argtypes = [P, P, P] + [i32] * 5 + [P, P, P, sz, P]
+        lib.csa_topk.restype = st
+        lib.csa_gather_swa.argtypes = [csa_cache_desc, P, i32, i32, P, P, P, i32, i32, i32, P, P, P]
+        lib.csa_gather_swa.restype = st
+        lib.csa_sink_attention_decode.argtypes = ([P, P, f32, csa_cache_desc, P, i32, i32, P, P, P, i32, i32, i32,
+                                                   P, P, P, sz, P])
+        lib.csa_sink_attention_decode.restype = st
+        lib.hca_sink_attention_decode.argtypes = ([P, P, f32, csa_cache_desc, P, P, i32, i32, P, i32, i32, i32,
+                                                   P, P, P, sz, P])
+        lib.hca_sink_attention_decode.restype = st
+        lib.csa_decode_step.argtypes = ([P] * 7 + [f32, csa_cache_desc, P, i32, i32, P, P] + [i32] * 5
+                                        + [P, P, P, P, P, sz, P])
+        lib.csa_decode_step.restype = st
+        lib.csa_read_device_error.argtypes = [C.POINTER(C.c_int32), P]
+        lib.csa_read_device_error.restype = st
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().csa_status_string(int(status)).decode()
+
+
+def csa_version() -> int:
+    return int(load().csa_version())
+
+
+def csa_kernel_launches() -> int:
+    """Kernels launched so far by this process through the library."""
+    return int(load().csa_kernel_launches())
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise CsaError(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: torch.Tensor | None, name: str, dtype=None, shape=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t.data_ptr()
+
+
+def cache_desc(records: torch.Tensor, seq_capacity: int, seq_stride: int = 0,
+               block_table: torch.Tensor | None = None, page_records: int = 0) -> csa_cache_desc:
+    """Describe a cache of latent records: ``records`` is uint8 [n, 592] (or
+    [B, Ncap, 592]); contiguous mode uses ``seq_stride``, paged mode a
+    ``block_table`` [B, max_pages] int32 and ``page_records``."""
+    rec = records.reshape(-1, RECORD_BYTES) if records.dim() != 2 else records
+    _ptr(rec, "records", torch.uint8)
+    if rec.shape[1] != RECORD_BYTES:
+        raise ValueError("records must be [n, 592] uint8")
+    d = csa_cache_desc()
+    d.base = rec.data_ptr()
+    d.n_records = rec.shape[0]
+    d.seq_stride = int(seq_stride)
+    d.seq_capacity = int(seq_capacity)
+    if block_table is not None:
+        _ptr(block_table, "block_table", torch.int32)
+        d.block_table = block_table.data_ptr()
+        d.page_records = int(page_records)
+        d.max_pages = int(block_table.shape[-1])
+    d._keepalive = (rec, block_table)  # noqa: SLF001
+    return d
+
+
+def csa_workspace_bytes(op: int, B: int, T: int, Ncap: int, k: int) -> int:
+    return int(load().csa_workspace_bytes(int(op), B, T, Ncap, k))
+
+
+def workspace(op: int, B: int, T: int, Ncap: int, k: int, device=None) -> torch.Tensor | None:
+    """Allocate (through PyTorch) a workspace of the size the library asks for."""
+    n = csa_workspace_bytes(op, B, T, Ncap, k)
+    if n == 0:
+        return None
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def csa_indexer_logits(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q_pos, n_comp, m: int,
+                       logits: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    B, T = q_pos.shape
+    Ncap = k_idx.shape[1]
+    if logits is None:
+        logits = torch.empty((B, T, Ncap), dtype=torch.float32, device=q_idx.device)
+    u8 = (torch.uint8, torch.float8_e4m3fn)
+    args = [_ptr(q_idx, "q_idx", u8, (B, T, IDX_HEADS, IDX_DIM)),
+            _ptr(q_idx_scale, "q_idx_scale", torch.float32, (B, T, IDX_HEADS)),
+            _ptr(w_idx, "w_idx", torch.float32, (B, T, IDX_HEADS)),
+            _ptr(k_idx, "k_idx", u8, (B, Ncap, IDX_DIM)),
+            _ptr(k_idx_scale, "k_idx_scale", torch.float32, (B, Ncap)),
+            _ptr(q_pos, "q_pos", torch.int32, (B, T)), _ptr(n_comp, "n_comp", torch.int32, (B,))]
+    _check(load().csa_indexer_logits(*args, B, T, Ncap, int(m),
+                                     _ptr(logits, "logits", torch.float32, (B, T, Ncap)), _stream(stream)),
+           "csa_indexer_logits")
+    return logits
+
+
+def csa_topk(logits, q_pos, n_comp, m: int, k: int, topk_idx=None, topk_cnt=None, ws=None, stream=None):
+    B, T, Ncap = logits.shape
+    dev = logits.device
+    if topk_idx is None:
+        topk_idx = torch.empty((B, T, k), dtype=torch.int32, device=dev)
+    if topk_cnt is None:
+        topk_cnt = torch.empty((B, T), dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = workspace(OP_TOPK, B, T, Ncap, k, dev)
+    _check(load().csa_topk(_ptr(logits, "logits", torch.float32), _ptr(q_pos, "q_pos", torch.int32, (B, T)),
+                           _ptr(n_comp, "n_comp", torch.int32, (B,)), B, T, Ncap, int(m), int(k),
+                           _ptr(topk_idx, "topk_idx", torch.int32, (B, T, k)),
+                           _ptr(topk_cnt, "topk_cnt", torch.int32, (B, T)),
+                           _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _stream(stream)),
+           "csa_topk")
+    return topk_idx, topk_cnt
+
+
+def csa_gather_swa(comp: csa_cache_desc, swa_ring, W: int, topk_idx, topk_cnt, q_pos, kv_out=None, kv_cnt=None,
+                   stream=None):
+    B, T, k = topk_idx.shape
+    R = swa_ring.shape[1]
+    dev = swa_ring.device
+    if kv_out is None:
+        kv_out = torch.empty((B, T, k + W, RECORD_BYTES), dtype=torch.uint8, device=dev)
+    if kv_cnt is None:
+        kv_cnt = torch.empty((B, T), dtype=torch.int32, device=dev)
+    _check(load().csa_gather_swa(comp, _ptr(swa_ring, "swa_ring", torch.uint8, (B, R, RECORD_BYTES)), R, int(W),
+                                 _ptr(topk_idx, "topk_idx", torch.int32), _ptr(topk_cnt, "topk_cnt", torch.int32, (B, T)),
+                                 _ptr(q_pos, "q_pos", torch.int32, (B, T)), B, T, k,
+                                 _ptr(kv_out, "kv_out", torch.uint8, (B, T, k + W, RECORD_BYTES)),
+                                 _ptr(kv_cnt, "kv_cnt", torch.int32, (B, T)), _stream(stream)), "csa_gather_swa")
+    return kv_out, kv_cnt
+
+
+def csa_sink_attention_decode(q, sink, softmax_scale: float, comp: csa_cache_desc, swa_ring, W: int, topk_idx,
+                              topk_cnt, q_pos, out=None, lse=None, ws=None, stream=None):
+    B, T = q_pos.shape
+    k = topk_idx.shape[2]
+    R = swa_ring.shape[1]
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, T, HEADS, DIM), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, T, HEADS), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(OP_ATTENTION, B, T, comp.seq_capacity, k, dev)
+    _check(load().csa_sink_attention_decode(
+        _ptr(q, "q", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(sink, "sink", torch.float32, (HEADS,)),
+        float(softmax_scale), comp, _ptr(swa_ring, "swa_ring", torch.uint8, (B, R, RECORD_BYTES)), R, int(W),
+        _ptr(topk_idx, "topk_idx", torch.int32, (B, T, k)), _ptr(topk_cnt, "topk_cnt", torch.int32, (B, T)),
+        _ptr(q_pos, "q_pos", torch.int32, (B, T)), B, T, k,
+        _ptr(out, "out", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(lse, "lse", torch.float32, (B, T, HEADS)),
+        _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _stream(stream)),
+        "csa_sink_attention_decode")
+    return out, lse
+
+
+def hca_sink_attention_decode(q, sink, softmax_scale: float, comp: csa_cache_desc, n_comp, swa_ring, W: int, q_pos,
+                              m_hca: int = 128, out=None, lse=None, ws=None, stream=None):
+    B, T = q_pos.shape
+    R = swa_ring.shape[1]
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, T, HEADS, DIM), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, T, HEADS), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(OP_HCA_ATTENTION, B, T, comp.seq_capacity, 0, dev)
+    _check(load().hca_sink_attention_decode(
+        _ptr(q, "q", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(sink, "sink", torch.float32, (HEADS,)),
+        float(softmax_scale), comp, _ptr(n_comp, "n_comp", torch.int32, (B,)),
+        _ptr(swa_ring, "swa_ring", torch.uint8, (B, R, RECORD_BYTES)), R, int(W),
+        _ptr(q_pos, "q_pos", torch.int32, (B, T)), B, T, int(m_hca),
+        _ptr(out, "out", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(lse, "lse", torch.float32, (B, T, HEADS)),
+        _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _stream(stream)),
+        "hca_sink_attention_decode")
+    return out, lse
+
+
+def csa_decode_step(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q, sink, softmax_scale: float,
+                    comp: csa_cache_desc, swa_ring, W: int, q_pos, n_comp, m: int, k: int, out=None, lse=None,
+                    topk_idx=None, topk_cnt=None, ws=None, stream=None):
+    B, T = q_pos.shape
+    Ncap = k_idx.shape[1]
+    R = swa_ring.shape[1]
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, T, HEADS, DIM), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, T, HEADS), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(OP_DECODE_STEP, B, T, Ncap, k, dev)
+    u8 = (torch.uint8, torch.float8_e4m3fn)
+    _check(load().csa_decode_step(
+        _ptr(q_idx, "q_idx", u8, (B, T, IDX_HEADS, IDX_DIM)),
+        _ptr(q_idx_scale, "q_idx_scale", torch.float32, (B, T, IDX_HEADS)),
+        _ptr(w_idx, "w_idx", torch.float32, (B, T, IDX_HEADS)), _ptr(k_idx, "k_idx", u8, (B, Ncap, IDX_DIM)),
+        _ptr(k_idx_scale, "k_idx_scale", torch.float32, (B, Ncap)),
+        _ptr(q, "q", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(sink, "sink", torch.float32, (HEADS,)),
+        float(softmax_scale), comp, _ptr(swa_ring, "swa_ring", torch.uint8, (B, R, RECORD_BYTES)), R, int(W),
+        _ptr(q_pos, "q_pos", torch.int32, (B, T)), _ptr(n_comp, "n_comp", torch.int32, (B,)),
+        B, T, Ncap, int(m), int(k),
+        _ptr(out, "out", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(lse, "lse", torch.float32, (B, T, HEADS)),
+        _ptr(topk_idx, "topk_idx", torch.int32, (B, T, k)), _ptr(topk_cnt, "topk_cnt", torch.int32, (B, T)),
+        _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _stream(stream)), "csa_decode_step")
+    return out, lse
+
+
+def csa_read_device_error(stream=None) -> int:
+    """Read and clear the device error word (synchronises the stream)."""
+    code = C.c_int32(0)
+    _check(load().csa_read_device_error(C.byref(code), _stream(stream)), "csa_read_device_error")
+    return int(code.value)

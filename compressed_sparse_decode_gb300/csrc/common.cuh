@@ -1,0 +1,102 @@
+// common.cuh -- shared device helpers of libcsa (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_fp16.h>
+
+#include "../../include/csa.h"
+
+namespace csa {
+
+constexpr int kHeads = CSA_HEADS;
+constexpr int kDim = CSA_LATENT_DIM;
+constexpr int kNope = CSA_NOPE_DIM;
+constexpr int kRope = CSA_ROPE_DIM;
+constexpr int kScaleBlock = CSA_SCALE_BLOCK;
+constexpr int kRecBytes = CSA_RECORD_BYTES;
+constexpr int kRopeOffset = kNope;                 // 448
+constexpr int kScaleOffset = kNope + 2 * kRope;    // 576
+constexpr int kIdxHeads = CSA_INDEXER_HEADS;
+constexpr int kIdxDim = CSA_INDEXER_DIM;
+
+// Host-side count of kernel launches issued by the library.
+void count_launch(int n = 1);
+
+// Records first set a sticky code in the per-device error word; the first
+// error wins.
+__device__ __forceinline__ void report_error(int *err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// Visible compressed entries of a query at 0-based position p: blocks strictly
+// before its own block floor(p/m), bounded by the stored entries and capacity
+// ("DSV4 Audit", section A3, item 1).
+__device__ __forceinline__ int visible_entries(int p, int m, int n_comp, int cap) {
+    if (p < 0) return 0;
+    int nv = p / m;
+    nv = nv < n_comp ? nv : n_comp;
+    nv = nv < cap ? nv : cap;
+    return nv < 0 ? 0 : nv;
+}
+
+// Device view of csa_cache_desc.
+struct CacheView {
+    const uint8_t *base;
+    int64_t n_records;
+    int64_t seq_stride;
+    const int32_t *block_table;
+    int32_t page_records;
+    int32_t max_pages;
+    int32_t seq_capacity;
+};
+
+inline CacheView make_view(const csa_cache_desc &d) {
+    CacheView v;
+    v.base = static_cast<const uint8_t *>(d.base);
+    v.n_records = d.n_records;
+    v.seq_stride = d.seq_stride;
+    v.block_table = d.block_table;
+    v.page_records = d.page_records;
+    v.max_pages = d.max_pages;
+    v.seq_capacity = d.seq_capacity;
+    return v;
+}
+
+// Physical record index of logical entry c of sequence b, or -1 outside the
+// cache (block-table strided, "ROADMAP -- Stage E", section E1).
+__device__ __forceinline__ int64_t record_index(const CacheView &v, int b, int c) {
+    if (c < 0 || c >= v.seq_capacity) return -1;
+    int64_t rec;
+    if (v.block_table) {
+        int page = c / v.page_records;
+        if (page >= v.max_pages) return -1;
+        int32_t phys = __ldg(v.block_table + (int64_t)b * v.max_pages + page);
+        if (phys < 0) return -1;
+        rec = (int64_t)phys * v.page_records + c % v.page_records;
+    } else {
+        rec = (int64_t)b * v.seq_stride + c;
+    }
+    return (rec >= 0 && rec < v.n_records) ? rec : -1;
+}
+
+// Two E4M3 codes (low byte first) -> two floats through the hardware
+// conversion (cvt e4m3x2 -> f16x2), exact.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+    return __half22float2(*reinterpret_cast<__half2 *>(&h));
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Order-preserving map of fp32 to uint32 (larger float -> larger key).
+__device__ __forceinline__ uint32_t order_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+}  // namespace csa

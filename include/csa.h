@@ -1,0 +1,223 @@
+/*
+ * csa.h -- C ABI of the GB300 (sm_103a) compressed sparse attention decode
+ * library, libcsa.so.
+ *
+ * One decode step of DSV4-style Compressed Sparse Attention (CSA), as the
+ * project's pages describe it:
+ *   1. lightning-indexer logits of each query token against every compressed
+ *      KV entry            -> csa_indexer_logits
+ *   2. top-k over the causally visible entries  -> csa_topk
+ *   3. gather of the selected FP8/BF16 latents together with the SWA window
+ *                          -> fused into step 4 (csa_gather_swa is the
+ *                             standalone packed gather)
+ *   4. one sink-merged attention pass  -> csa_sink_attention_decode
+ * and the heavily-compressed (HCA) variant that attends to every visible entry
+ * with no indexer -> hca_sink_attention_decode. csa_decode_step runs 1, 2, 4.
+ *
+ * Conventions for every call
+ *  - Pointers are DEVICE pointers unless stated; the caller owns all memory.
+ *    The library allocates nothing. It keeps one device-side error word per
+ *    device (see csa_read_device_error) and per-process kernel attributes.
+ *  - Calls are asynchronous on `stream`; none synchronises the device.
+ *    Argument errors are detected on the host before any launch and returned
+ *    as codes; launch failures return CSA_ERR_CUDA (cudaGetLastError).
+ *  - Index or position data that would address memory outside a cache is
+ *    detected in the kernels: the access is skipped and CSA_ERR_BAD_INDEX is
+ *    recorded in the device error word. Kernels never trap.
+ *  - Shapes fixed by the method: H = 128 query heads, latent D = 512 = 448
+ *    FP8 E4M3 "nope" dims + 64 BF16 rope dims, indexer Hi = 64 heads x Di = 128
+ *    FP8 dims. Tensors are dense row-major in the order of their index lists.
+ *  - Every pointer must be 16-byte aligned.
+ *
+ * Latent record (one compressed entry or one SWA token), CSA_RECORD_BYTES:
+ *   bytes [0,448)   nope dims, FP8 E4M3
+ *   bytes [448,576) rope dims, BF16
+ *   bytes [576,592) 4 fp32 dequantisation multipliers; multiplier i covers
+ *                   nope dims [128i, min(128i+128, 448))
+ * (pages: "DSV4 Audit", section B1 -- FP8 nope + BF16 rope, fed to attention
+ * without a BF16 dequantised copy; "ROADMAP -- Stage E", section E1 -- FP8
+ * entries with the inverse scale stored alongside.)
+ */
+#ifndef CSA_H_
+#define CSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define CSA_API __attribute__((visibility("default")))
+#else
+#define CSA_API
+#endif
+
+#define CSA_HEADS 128
+#define CSA_LATENT_DIM 512
+#define CSA_NOPE_DIM 448
+#define CSA_ROPE_DIM 64
+#define CSA_SCALE_BLOCK 128
+#define CSA_RECORD_BYTES 592
+#define CSA_INDEXER_HEADS 64
+#define CSA_INDEXER_DIM 128
+#define CSA_MAX_TOKENS_PER_SEQ 4 /* T: query tokens per sequence and step */
+#define CSA_MAX_TOPK 2048
+#define CSA_MAX_SWA_WINDOW 512 /* W */
+
+typedef enum {
+    CSA_OK = 0,
+    CSA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, size out of range */
+    CSA_ERR_UNSUPPORTED = 2, /* a shape outside what the kernels implement */
+    CSA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
+    CSA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+    CSA_ERR_TIMEOUT = 5,     /* (device word) a bounded wait in a kernel expired */
+    CSA_ERR_BAD_INDEX = 6    /* (device word) an index/position outside a cache */
+} csa_status_t;
+
+/* A cache of latent records (compressed entries). Logical entry c of sequence
+ * b (0 <= c < seq_capacity) is record
+ *     b * seq_stride + c                                     if block_table == NULL
+ *     block_table[b*max_pages + c/page_records]*page_records + c%page_records
+ * ("DSV4 Inference Kernel" README, Architecture: classical paged cache of
+ * 128-token pages, i.e. 32 CSA entries or 1 HCA entry per page).
+ * Records outside [0, n_records) are never read. */
+typedef struct {
+    const void *base;           /* device, n_records * CSA_RECORD_BYTES bytes */
+    int64_t n_records;          /* records addressable from base */
+    int64_t seq_stride;         /* contiguous mode: records between sequences */
+    const int32_t *block_table; /* device [B, max_pages] or NULL */
+    int32_t page_records;       /* paged mode: records per page (> 0) */
+    int32_t max_pages;          /* paged mode: block-table row length */
+    int32_t seq_capacity;       /* logical entries per sequence (Ncap) */
+} csa_cache_desc;
+
+typedef enum {
+    CSA_OP_INDEXER = 0,
+    CSA_OP_TOPK = 1,
+    CSA_OP_ATTENTION = 2,     /* csa_sink_attention_decode, `k` = top-k */
+    CSA_OP_HCA_ATTENTION = 3, /* hca_sink_attention_decode, `k` ignored */
+    CSA_OP_DECODE_STEP = 4    /* csa_decode_step */
+} csa_op_t;
+
+/* Workspace bytes that `op` needs for these sizes (0 if none). A workspace
+ * passed to a call must be at least this large and 256-byte aligned; its
+ * contents need no initialisation and are scratch between calls. */
+CSA_API size_t csa_workspace_bytes(csa_op_t op, int B, int T, int Ncap, int k);
+
+/* Step 1 -- lightning-indexer logits ("DSV4 Audit", section B2: weighted-ReLU
+ * MQA logits of every query token against every compressed entry, FP8 keys).
+ *   logits[b,t,c] = sum_h w_idx[b,t,h] *
+ *                   max(0, q_idx_scale[b,t,h] * k_idx_scale[b,c] *
+ *                          sum_d e4m3(q_idx[b,t,h,d]) * e4m3(k_idx[b,c,d]))
+ * for c < n_vis(b,t), and -inf for n_vis(b,t) <= c < Ncap, where
+ *   n_vis(b,t) = min(floor(q_pos[b,t] / m), n_comp[b], Ncap)
+ * ("DSV4 Audit", section A3 item 1: a query sees only the compressed blocks
+ * strictly before its own incomplete block; q_pos is the 0-based position).
+ *   q_idx       [B,T,64,128] e4m3 codes     q_idx_scale [B,T,64] fp32 (> 0)
+ *   w_idx       [B,T,64] fp32               k_idx [B,Ncap,128] e4m3 codes
+ *   k_idx_scale [B,Ncap] fp32 (> 0)          q_pos [B,T] int32, n_comp [B] int32
+ *   logits      [B,T,Ncap] fp32 (written in full)
+ * Requires 1 <= T <= 4, Ncap >= 1, m >= 1. Accumulation is fp32. */
+CSA_API csa_status_t csa_indexer_logits(const uint8_t *q_idx, const float *q_idx_scale, const float *w_idx,
+                                const uint8_t *k_idx, const float *k_idx_scale,
+                                const int32_t *q_pos, const int32_t *n_comp,
+                                int B, int T, int Ncap, int m, float *logits, cudaStream_t stream);
+
+/* Step 2 -- top-k of the indexer logits over the visible entries ("DSV4
+ * Audit", section B2 and "ROADMAP -- Stage E", section E7: top-k per query
+ * token with warp-level reductions and no global lock).
+ * For each (b,t): the min(k, n_vis) entries c < n_vis with the largest
+ * logits, ties going to the lower index, written to topk_idx[b,t,0..cnt) in
+ * ascending index order, the rest of the row set to -1; topk_cnt[b,t] = cnt.
+ *   logits [B,T,Ncap] fp32 (entries >= n_vis are not read), topk_idx [B,T,k]
+ *   int32, topk_cnt [B,T] int32. Requires 1 <= k <= min(Ncap, CSA_MAX_TOPK).
+ * The workspace may be NULL when csa_workspace_bytes(CSA_OP_TOPK, ...) is 0. */
+CSA_API csa_status_t csa_topk(const float *logits, const int32_t *q_pos, const int32_t *n_comp,
+                      int B, int T, int Ncap, int m, int k, int32_t *topk_idx, int32_t *topk_cnt,
+                      void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Step 3, standalone -- packed candidate records ("DSV4 Audit", section A3:
+ * the query attends to [top-k compressed entries] ++ [SWA window]; a token in
+ * both is kept twice; "ROADMAP -- Stage E", section E1: gathers straight from
+ * the FP8 cache, block-table strided).
+ * For each (b,t) with p = q_pos[b,t]: kv_out[b,t,i] = comp entry
+ * topk_idx[b,t,i] for i < topk_cnt[b,t], followed by the SWA records of
+ * positions max(0,p-W+1) .. p (oldest first), position j read from
+ * swa_ring[b, j mod R]; kv_cnt[b,t] = number written. Slots past kv_cnt are
+ * not written. Byte-exact copies, no dequantisation.
+ *   swa_ring [B,R,592] bytes, kv_out [B,T,k+W,592] bytes, kv_cnt [B,T] int32.
+ * Requires 1 <= W <= R and q_pos >= 0. The caller keeps the ring holding the
+ * window of every query token (R >= W + T - 1 for consecutive tokens). */
+CSA_API csa_status_t csa_gather_swa(csa_cache_desc comp, const void *swa_ring, int R, int W,
+                            const int32_t *topk_idx, const int32_t *topk_cnt, const int32_t *q_pos,
+                            int B, int T, int k, void *kv_out, int32_t *kv_cnt, cudaStream_t stream);
+
+/* Step 4 -- sink-merged attention over [top-k entries] ++ [SWA window]
+ * ("DSV4 Inference Kernel" README, Architecture: one 512-d latent per entry
+ * shared by all 128 heads as key and value; sink weights merge the sparse and
+ * SWA terms). With x_j the dequantised candidate latents (nope code times
+ * its block multiplier, rope as BF16), for every head h:
+ *   z_j   = softmax_scale * sum_d q[b,t,h,d] * x_j[d]
+ *   M     = max(sink[h], max_j z_j)
+ *   den   = exp(sink[h] - M) + sum_j exp(z_j - M)
+ *   out   = sum_j exp(z_j - M) x_j / den       (BF16)
+ *   lse   = M + ln(den)                         (fp32)
+ * No candidates: out = 0 and lse = sink[h].
+ *   q [B,T,128,512] bf16, sink [128] fp32, out [B,T,128,512] bf16,
+ *   lse [B,T,128] fp32; other arguments as in csa_gather_swa.
+ * The candidates are read straight from the caches (no packed copy). */
+CSA_API csa_status_t csa_sink_attention_decode(const void *q, const float *sink, float softmax_scale,
+                                       csa_cache_desc comp, const void *swa_ring, int R, int W,
+                                       const int32_t *topk_idx, const int32_t *topk_cnt,
+                                       const int32_t *q_pos, int B, int T, int k,
+                                       void *out, float *lse, void *workspace, size_t workspace_bytes,
+                                       cudaStream_t stream);
+
+/* HCA variant ("DSV4 Inference Kernel" README, Architecture, m' = 128;
+ * "ROADMAP -- Stage E", section E1, gather of all compressed entries):
+ * step 4 with the candidates = every visible entry c < n_vis(b,t) (computed
+ * with m = m_hca as in csa_indexer_logits) ++ the SWA window. No indexer. */
+CSA_API csa_status_t hca_sink_attention_decode(const void *q, const float *sink, float softmax_scale,
+                                       csa_cache_desc comp, const int32_t *n_comp,
+                                       const void *swa_ring, int R, int W, const int32_t *q_pos,
+                                       int B, int T, int m_hca, void *out, float *lse,
+                                       void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* One CSA decode step: csa_indexer_logits -> csa_topk ->
+ * csa_sink_attention_decode on one stream. Logits, indices and attention
+ * scratch live in the workspace (csa_workspace_bytes(CSA_OP_DECODE_STEP,...)).
+ * The indexer keys are contiguous per sequence ([B,Ncap,...]); comp may be
+ * paged. Arguments keep the meaning given above. topk_idx/topk_cnt may be
+ * NULL; if given ([B,T,k] / [B,T]) they receive the selection. */
+CSA_API csa_status_t csa_decode_step(const uint8_t *q_idx, const float *q_idx_scale, const float *w_idx,
+                             const uint8_t *k_idx, const float *k_idx_scale,
+                             const void *q, const float *sink, float softmax_scale,
+                             csa_cache_desc comp, const void *swa_ring, int R, int W,
+                             const int32_t *q_pos, const int32_t *n_comp,
+                             int B, int T, int Ncap, int m, int k,
+                             void *out, float *lse, int32_t *topk_idx, int32_t *topk_cnt,
+                             void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Reads and clears the current device's error word (CSA_OK or the first
+ * CSA_ERR_TIMEOUT / CSA_ERR_BAD_INDEX recorded by a kernel). Blocking: it
+ * synchronises `stream`. For tests and diagnostics, not for the hot path. */
+CSA_API csa_status_t csa_read_device_error(int32_t *host_code, cudaStream_t stream);
+
+/* Static description of a status code. */
+CSA_API const char *csa_status_string(csa_status_t status);
+
+/* Number of kernels this process has launched through the library (all
+ * devices, all streams; a host-side counter incremented at every launch). */
+CSA_API uint64_t csa_kernel_launches(void);
+
+/* Library ABI version (major * 100 + minor). */
+CSA_API int csa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_H_ */

@@ -1,0 +1,93 @@
+"""The C-ABI library builds, loads and exports every symbol include/csa.h
+declares; host-side validation rejects bad arguments before any launch.
+No test here needs a GPU (no call reaches a kernel)."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+import compressed_sparse_decode_gb300 as csd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    csd.build()
+    return csd.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "csa.h")).read()
+    return sorted(set(re.findall(r"CSA_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_names():
+    assert _declared() == sorted(csd.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", csd.LIB], capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in _declared():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    # nothing else leaks out of the library's C namespace
+    assert not [s for s in exported if s.startswith("csa") and s not in _declared()]
+
+
+def test_version_and_status_strings(lib):
+    assert csd.csa_version() == 100
+    assert csd.status_string(csd.OK) == "ok"
+    assert "workspace" in csd.status_string(csd.ERR_WORKSPACE)
+    assert csd.status_string(99) == "unknown status"
+
+
+def test_workspace_sizes(lib):
+    assert csd.csa_workspace_bytes(csd.OP_INDEXER, 32, 1, 32768, 2048) == 0
+    step = csd.csa_workspace_bytes(csd.OP_DECODE_STEP, 32, 1, 32768, 2048)
+    assert step >= 4 * 32 * 32768 + 2 * 4 * 32 * 2048
+    assert step % 256 == 0
+    assert csd.csa_workspace_bytes(csd.OP_TOPK, 0, 1, 10, 1) == 0
+
+
+def test_host_validation_rejects_before_launch(lib):
+    P = C.c_void_p
+    fake = P(0x1000)  # never dereferenced: validation fails first
+    # null pointers
+    assert lib.csa_indexer_logits(None, None, None, None, None, None, None, 1, 1, 8, 4, None, None) == csd.ERR_INVALID_ARG
+    # T beyond the supported maximum
+    assert lib.csa_indexer_logits(fake, fake, fake, fake, fake, fake, fake, 1, 5, 8, 4, fake, None) == csd.ERR_INVALID_ARG
+    # misaligned logits pointer
+    assert lib.csa_indexer_logits(fake, fake, fake, fake, fake, fake, fake, 1, 1, 8, 4, P(0x1004), None) == csd.ERR_INVALID_ARG
+    # k larger than the capacity / the maximum
+    assert lib.csa_topk(fake, fake, fake, 1, 1, 8, 4, 9, fake, fake, None, 0, None) == csd.ERR_UNSUPPORTED
+    assert lib.csa_topk(fake, fake, fake, 1, 1, 10000, 4, 4096, fake, fake, None, 0, None) == csd.ERR_UNSUPPORTED
+    # cache descriptor without records, window larger than the ring
+    bad = csd.csa_cache_desc()
+    assert lib.csa_gather_swa(bad, fake, 128, 128, fake, fake, fake, 1, 1, 4, fake, fake, None) == csd.ERR_INVALID_ARG
+    good = csd.csa_cache_desc()
+    good.base, good.n_records, good.seq_stride, good.seq_capacity = 0x1000, 10, 10, 10
+    assert lib.csa_gather_swa(good, fake, 64, 128, fake, fake, fake, 1, 1, 4, fake, fake, None) == csd.ERR_INVALID_ARG
+    # contiguous mode with overlapping sequences
+    over = csd.csa_cache_desc()
+    over.base, over.n_records, over.seq_stride, over.seq_capacity = 0x1000, 100, 5, 10
+    assert lib.csa_gather_swa(over, fake, 128, 128, fake, fake, fake, 2, 1, 4, fake, fake, None) == csd.ERR_INVALID_ARG
+    # non-positive softmax scale
+    assert lib.csa_sink_attention_decode(fake, fake, C.c_float(0.0), good, fake, 128, 128, fake, fake, fake, 1, 1, 4,
+                                         fake, fake, None, 0, None) == csd.ERR_INVALID_ARG
+    # decode step without workspace
+    assert lib.csa_decode_step(fake, fake, fake, fake, fake, fake, fake, C.c_float(0.1), good, fake, 128, 128, fake,
+                               fake, 1, 1, 10, 4, 4, fake, fake, None, None, None, 0, None) == csd.ERR_WORKSPACE
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "compressed_sparse_decode_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "csa_oracle" not in text, f

@@ -1,0 +1,155 @@
+"""GPU edge cases against the oracle: ragged capacities spanning several tiles
+with a ragged tail, T up to 4 with per-token visible ranges, empty visible
+ranges, windows shorter than W, k above the visible count, paged caches with
+a shuffled block table, heavy ties in top-k, a -inf sink, and indices outside
+the cache (reported through the device error word, never dereferenced)."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _parity import (check_attention, check_logits, check_topk_exact, logit_magnitude, oracle_cache)
+
+pytestmark = pytest.mark.gpu
+THREADS = os.cpu_count() or 1
+SCALE = 1.0 / math.sqrt(512)
+
+
+def _custom(B, T, ncap, k, q_pos, n_comp, paged=False, seed=3):
+    wl = synth.custom("csa", B=B, T=T, ncap=ncap, k=k, ctx=1 << 20)
+    x = synth.generate(wl, seed=seed, device="cuda", paged=paged)
+    x.q_pos = torch.tensor(q_pos, dtype=torch.int32, device="cuda")
+    x.n_comp = torch.tensor(n_comp, dtype=torch.int32, device="cuda")
+    return x
+
+
+def _cache(csd, x):
+    return csd.cache_desc(x.comp, x.wl.ncap, x.seq_stride, x.block_table,
+                          x.page_records if x.block_table is not None else 0)
+
+
+# q_pos chosen so that n_vis = floor(p/4) covers 0, < k, = k, > k and the
+# capacity, and windows shorter than W = 128
+EDGE_POS = [[0, 1, 2, 3], [5, 6, 7, 8], [130, 131, 132, 133], [1199, 1200, 1201, 1202], [257, 258, 259, 260]]
+EDGE_NCOMP = [300, 300, 300, 300, 64]
+
+
+def _pipeline(csd, x):
+    lg = csd.csa_indexer_logits(x.q_idx, x.q_idx_scale, x.w_idx, x.k_idx, x.k_idx_scale, x.q_pos, x.n_comp, x.wl.m)
+    idx, cnt = csd.csa_topk(lg, x.q_pos, x.n_comp, x.wl.m, x.wl.k)
+    return lg, idx, cnt
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+def test_ragged_capacity_and_visibility(cuda_lib, T):
+    pos = [row[:T] for row in EDGE_POS]
+    x = _custom(5, T, 300, 40, pos, EDGE_NCOMP)
+    lg, idx, cnt = _pipeline(cuda_lib, x)
+    assert cuda_lib.csa_read_device_error() == 0
+    rows = list(range(5 * T))
+    ora = oracle.indexer_logits(x.q_idx.cpu(), x.q_idx_scale.cpu(), x.w_idx.cpu(), x.k_idx.cpu(),
+                                x.k_idx_scale.cpu(), x.q_pos.cpu(), x.n_comp.cpu(), 4, threads=THREADS)
+    A = logit_magnitude(x, rows)
+    g = lg.cpu().numpy().reshape(-1, 300)
+    for r in rows:
+        check_logits(g[r], ora.reshape(-1, 300)[r], A[r], f"T={T} row {r}")
+    oi, oc = oracle.topk(lg.cpu().numpy().astype(np.float64), x.q_pos.cpu(), x.n_comp.cpu(), 4, 40)
+    check_topk_exact(idx.cpu().numpy(), cnt.cpu().numpy(), oi, oc, f"T={T}")
+    out, lse = cuda_lib.csa_sink_attention_decode(x.q, x.sink, SCALE, _cache(cuda_lib, x), x.ring, 128, idx, cnt,
+                                                  x.q_pos)
+    assert cuda_lib.csa_read_device_error() == 0
+    oo, ol = oracle.csa_attention(x.q.view(torch.int16).cpu(), x.sink.cpu(), SCALE, oracle_cache(x),
+                                  x.ring.cpu().numpy(), 128, idx.cpu(), cnt.cpu(), x.q_pos.cpu(), threads=THREADS)
+    check_attention(out.float().cpu().numpy().reshape(-1, 128, 512), lse.cpu().numpy().reshape(-1, 128),
+                    oo.reshape(-1, 128, 512), ol.reshape(-1, 128), f"T={T}")
+    kv, kvc = cuda_lib.csa_gather_swa(_cache(cuda_lib, x), x.ring, 128, idx, cnt, x.q_pos)
+    okv, okc = oracle.gather(oracle_cache(x), x.ring.cpu().numpy(), 128, idx.cpu(), cnt.cpu(), x.q_pos.cpu())
+    assert np.array_equal(kvc.cpu().numpy(), okc)
+    gkv = kv.cpu().numpy()
+    for r in np.ndindex(*okc.shape):
+        assert np.array_equal(gkv[r][:okc[r]], okv[r][:okc[r]])
+
+
+def test_indexer_capacity_not_a_multiple_of_the_tile(cuda_lib):
+    for ncap in (1, 127, 129, 1000):
+        x = _custom(2, 1, ncap, 1, [[4 * ncap + 8], [4 * ncap - 4]], [ncap, ncap])
+        lg = cuda_lib.csa_indexer_logits(x.q_idx, x.q_idx_scale, x.w_idx, x.k_idx, x.k_idx_scale, x.q_pos, x.n_comp, 4)
+        ora = oracle.indexer_logits(x.q_idx.cpu(), x.q_idx_scale.cpu(), x.w_idx.cpu(), x.k_idx.cpu(),
+                                    x.k_idx_scale.cpu(), x.q_pos.cpu(), x.n_comp.cpu(), 4)
+        A = logit_magnitude(x, [0, 1])
+        for r in (0, 1):
+            check_logits(lg.cpu().numpy().reshape(-1, ncap)[r], ora.reshape(-1, ncap)[r], A[r], f"ncap={ncap}")
+
+
+def test_paged_cache_matches_contiguous_and_oracle(cuda_lib):
+    pos = [[1023, 1024], [4000, 4001]]
+    xc = _custom(2, 2, 1000, 64, pos, [1000, 1000], paged=False, seed=7)
+    xp = _custom(2, 2, 1000, 64, pos, [1000, 1000], paged=True, seed=7)
+    assert xp.block_table is not None
+    _, idx, cnt = _pipeline(cuda_lib, xc)
+    oc_, lc_ = cuda_lib.csa_sink_attention_decode(xc.q, xc.sink, SCALE, _cache(cuda_lib, xc), xc.ring, 128, idx, cnt,
+                                                  xc.q_pos)
+    op_, lp_ = cuda_lib.csa_sink_attention_decode(xp.q, xp.sink, SCALE, _cache(cuda_lib, xp), xp.ring, 128, idx, cnt,
+                                                  xp.q_pos)
+    assert cuda_lib.csa_read_device_error() == 0
+    assert torch.equal(oc_, op_) and torch.equal(lc_, lp_)
+    oo, ol = oracle.csa_attention(xp.q.view(torch.int16).cpu(), xp.sink.cpu(), SCALE, oracle_cache(xp),
+                                  xp.ring.cpu().numpy(), 128, idx.cpu(), cnt.cpu(), xp.q_pos.cpu(), threads=THREADS)
+    check_attention(op_.float().cpu().numpy().reshape(-1, 128, 512), lp_.cpu().numpy().reshape(-1, 128),
+                    oo.reshape(-1, 128, 512), ol.reshape(-1, 128), "paged")
+    kv, kvc = cuda_lib.csa_gather_swa(_cache(cuda_lib, xp), xp.ring, 128, idx, cnt, xp.q_pos)
+    okv, okc = oracle.gather(oracle_cache(xp), xp.ring.cpu().numpy(), 128, idx.cpu(), cnt.cpu(), xp.q_pos.cpu())
+    assert np.array_equal(kvc.cpu().numpy(), okc)
+    for r in np.ndindex(*okc.shape):
+        assert np.array_equal(kv.cpu().numpy()[r][:okc[r]], okv[r][:okc[r]])
+
+
+def test_topk_heavy_ties_and_extremes(cuda_lib):
+    rng = np.random.default_rng(0)
+    B, T, ncap = 3, 2, 5000
+    vals = rng.integers(-5, 6, size=(B, T, ncap)).astype(np.float32)
+    vals[0, 0, 100:200] = 1e30
+    vals[1, 1, :] = 0.0                       # all equal: lowest indices win
+    vals[2, 0, ::7] = -np.float32(np.inf)
+    lg = torch.tensor(vals, device="cuda")
+    q_pos = torch.tensor([[20000, 20001], [19996, 19999], [400, 401]], dtype=torch.int32, device="cuda")
+    n_comp = torch.tensor([ncap, ncap, ncap], dtype=torch.int32, device="cuda")
+    for k in (1, 7, 64, 1000, 2048):
+        idx, cnt = cuda_lib.csa_topk(lg, q_pos, n_comp, 4, k)
+        oi, oc = oracle.topk(vals.astype(np.float64), q_pos.cpu(), n_comp.cpu(), 4, k)
+        check_topk_exact(idx.cpu().numpy(), cnt.cpu().numpy(), oi, oc, f"ties k={k}")
+
+
+def test_single_candidate_with_minus_inf_sink(cuda_lib):
+    # HCA, query at position 0: no visible entry, a window of one token, and a
+    # sink of -inf -> every head returns that token's latent (BF16-rounded)
+    wl = synth.custom("hca", B=2, T=1, ncap=16, k=0, ctx=0)
+    x = synth.generate(wl, seed=5, device="cuda")
+    x.q_pos = torch.zeros((2, 1), dtype=torch.int32, device="cuda")
+    sink = torch.full((128,), -float("inf"), device="cuda")
+    out, lse = cuda_lib.hca_sink_attention_decode(x.q, sink, SCALE, _cache(cuda_lib, x), x.n_comp, x.ring, 128,
+                                                  x.q_pos, 128)
+    oo, ol = oracle.hca_attention(x.q.view(torch.int16).cpu(), sink.cpu(), SCALE, oracle_cache(x), x.n_comp.cpu(),
+                                  x.ring.cpu().numpy(), 128, x.q_pos.cpu(), 128)
+    xv = oo[:, 0, 0, :]                                 # the dequantised slot-0 latent of each sequence
+    for h in range(128):
+        assert np.array_equal(oo[:, 0, h], xv)
+    got = out.float().cpu().numpy()[:, 0]
+    assert np.all(np.abs(got - xv[:, None, :]) <= 2.0 ** -8 * np.abs(xv[:, None, :]) + 1e-30)
+    np.testing.assert_allclose(lse.cpu().numpy()[:, 0], ol[:, 0], atol=2e-3)
+
+
+def test_out_of_cache_index_is_reported_not_read(cuda_lib):
+    x = _custom(1, 1, 64, 4, [[1000]], [64])
+    idx = torch.tensor([[[3, 64, 1 << 30, -5]]], dtype=torch.int32, device="cuda")
+    cnt = torch.tensor([[4]], dtype=torch.int32, device="cuda")
+    assert cuda_lib.csa_read_device_error() == 0
+    cuda_lib.csa_sink_attention_decode(x.q, x.sink, SCALE, _cache(cuda_lib, x), x.ring, 128, idx, cnt, x.q_pos)
+    assert cuda_lib.csa_read_device_error() == cuda_lib.ERR_BAD_INDEX
+    cuda_lib.csa_gather_swa(_cache(cuda_lib, x), x.ring, 128, idx, cnt, x.q_pos)
+    assert cuda_lib.csa_read_device_error() == cuda_lib.ERR_BAD_INDEX
+    assert cuda_lib.csa_read_device_error() == 0   # reading clears the word
