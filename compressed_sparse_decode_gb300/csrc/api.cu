@@ -10,7 +10,7 @@
 
 namespace csa {
 cudaError_t launch_indexer(const uint8_t *, const float *, const float *, const uint8_t *, const float *,
-                           const int32_t *, const int32_t *, int, int, int, int, float *, cudaStream_t);
+                           const int32_t *, const int32_t *, int, int, int, int, float *, int *, cudaStream_t);
 size_t topk_workspace_bytes(int, int, int, int);
 cudaError_t launch_topk(const float *, const int32_t *, const int32_t *, int, int, int, int, int, int32_t *,
                         int32_t *, void *, size_t, cudaStream_t);
@@ -119,8 +119,9 @@ csa_status_t csa_indexer_logits(const uint8_t *q_idx, const float *q_idx_scale, 
         !aligned16(w_idx) || !aligned16(k_idx_scale))
         return CSA_ERR_INVALID_ARG;
     if (!valid_dims(B, T) || Ncap < 1 || m < 1) return CSA_ERR_INVALID_ARG;
+    if ((int64_t)B * Ncap >= ((int64_t)1 << 31)) return CSA_ERR_UNSUPPORTED;
     return cuda_status(launch_indexer(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q_pos, n_comp, B, T, Ncap, m,
-                                      logits, stream));
+                                      logits, device_error_word(), stream));
 }
 
 csa_status_t csa_topk(const float *logits, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap,

@@ -1,102 +1,348 @@
-// indexer.cu -- lightning-indexer logits ("DSV4 Audit", section B2).
+// indexer.cu -- lightning-indexer logits on the FP8 tensor cores
+// ("DSV4 Audit", section B2: weighted-ReLU MQA logits of every query token
+// against every compressed entry, FP8 keys, on tensor cores rather than an
+// fp32 einsum).
 //
-// logits[b,t,c] = sk[b,c] * sum_h (w[b,t,h] * sq[b,t,h]) * relu(sum_d q8[b,t,h,d] k8[b,c,d])
-// which equals the weighted-ReLU form because the scales are positive.
-// Entries c >= n_vis(b,t) get -inf ("DSV4 Audit", section A3, item 1).
+//   logits[b,t,c] = sk[b,c] * sum_h (w[b,t,h] * sq[b,t,h]) * relu(sum_d q8[b,t,h,d] k8[b,c,d])
+//
+// which is the weighted-ReLU form because the FP8 scales are positive. Entries
+// c >= n_vis(b,t) get -inf ("DSV4 Audit", section A3, item 1).
+//
+// Design (one persistent CTA per SM, 6 warps):
+//   warp 0   TMA producer: 128-key x 128-byte FP8 tiles (128-byte swizzle) into
+//            an 8-stage shared-memory ring; per sequence, the T*64 query rows
+//            (FP8) and the head weights w*sq into one of two query slots.
+//   warp 1   MMA issuer: tcgen05.mma kind::f8f6f4, M = 128 keys, N = 64*T
+//            query-head rows, K = 128 (4 x K32), fp32 accumulator in TMEM,
+//            two accumulator buffers so the epilogue overlaps the next tile.
+//   warps 2-5 epilogue: thread i owns TMEM lane i = key c0+i; it reads the
+//            64*T head dot products, applies ReLU and the head weights, scales
+//            by the key's scale and writes the row of logits (coalesced).
+// Keys are read once from HBM for all T tokens of a sequence; tiles past the
+// largest visible range of their sequence are never loaded (written -inf).
+// Every wait is bounded; a timeout records CSA_ERR_TIMEOUT and the CTA exits
+// after its copies and MMAs have drained.
+#include <cuda.h>
+
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace csa {
 
 namespace {
 
-constexpr int kKeysPerCta = 128;
+constexpr int kTileKeys = 128;
+constexpr int kStages = 8;
+constexpr int kTileBytes = kTileKeys * kIdxDim;  // 16 KB
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
-// One thread per key. Query codes (exact as floats) and the per-head weights
-// w*sq for every token of the sequence sit in shared memory; each key's 128
-// codes sit in registers.
-__global__ void __launch_bounds__(kKeysPerCta)
-indexer_simt_kernel(const uint8_t *__restrict__ q_idx, const float *__restrict__ q_scale,
-                    const float *__restrict__ w_idx, const uint8_t *__restrict__ k_idx,
-                    const float *__restrict__ k_scale, const int32_t *__restrict__ q_pos,
-                    const int32_t *__restrict__ n_comp, int T, int Ncap, int m,
-                    float *__restrict__ logits) {
-    extern __shared__ float4 smem4[];
-    float *qf = reinterpret_cast<float *>(smem4);          // [T][64][128]
-    float *ws = qf + T * kIdxHeads * kIdxDim;              // [T][64]
-    __shared__ int nvis[CSA_MAX_TOKENS_PER_SEQ];
+template <int T>
+struct IdxSmem {
+    static constexpr int kQBytes = T * kIdxHeads * kIdxDim;  // T * 8 KB
+    alignas(1024) uint8_t keys[kStages][kTileBytes];
+    alignas(1024) uint8_t q[2][kQBytes];
+    float ws[2][T * kIdxHeads];  // w * sq per query slot
+    uint64_t full[kStages], empty[kStages];
+    uint64_t acc_full[2], acc_empty[2];
+    uint64_t q_full[2], q_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+};
 
-    const int b = blockIdx.y;
-    const int tid = threadIdx.x;
-    const uint8_t *qb = q_idx + (size_t)b * T * kIdxHeads * kIdxDim;
-    for (int i = tid * 2; i < T * kIdxHeads * kIdxDim; i += blockDim.x * 2) {
-        float2 v = e4m3x2_to_float2(*reinterpret_cast<const uint16_t *>(qb + i));
-        qf[i] = v.x;
-        qf[i + 1] = v.y;
+struct TileInfo {
+    int b;
+    int c0;
+    bool skip;
+};
+
+__device__ __forceinline__ int seq_visible_max(const int32_t *q_pos, const int32_t *n_comp, int b, int T, int m,
+                                               int Ncap) {
+    int nv = 0;
+    for (int t = 0; t < T; ++t) nv = max(nv, visible_entries(__ldg(q_pos + b * T + t), m, __ldg(n_comp + b), Ncap));
+    return nv;
+}
+
+template <int T>
+__global__ void __launch_bounds__(kThreads, 1)
+indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                  const float *__restrict__ q_scale, const float *__restrict__ w_idx,
+                  const float *__restrict__ k_scale, const int32_t *__restrict__ q_pos,
+                  const int32_t *__restrict__ n_comp, int B, int Ncap, int m, float *__restrict__ logits, int *err) {
+    constexpr int N = T * kIdxHeads;
+    constexpr uint32_t kTmemCols = (2 * N <= 128) ? 128 : (2 * N <= 256 ? 256 : 512);
+    constexpr uint32_t kIdesc = ptx::idesc_f32acc(0, 0, kTileKeys, N);
+    extern __shared__ uint8_t smem_raw[];
+    IdxSmem<T> &s = *reinterpret_cast<IdxSmem<T> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_tiles = (Ncap + kTileKeys - 1) / kTileKeys;
+    const long total = (long)B * n_tiles;
+    const long t_begin = total * blockIdx.x / gridDim.x;
+    const long t_end = total * (blockIdx.x + 1) / gridDim.x;
+    volatile int *abort = &s.abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            ptx::mbar_init(&s.full[i], 1);
+            ptx::mbar_init(&s.empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&s.acc_full[i], 1);
+            ptx::mbar_init(&s.acc_empty[i], 4);
+            ptx::mbar_init(&s.q_full[i], 1 + 32);
+            ptx::mbar_init(&s.q_empty[i], 1 + 4);
+        }
+        ptx::mbar_init(&s.mma_done, 1);
+        s.abort_flag = 0;
+        ptx::fence_mbar_init();
     }
-    for (int i = tid; i < T * kIdxHeads; i += blockDim.x)
-        ws[i] = w_idx[(size_t)b * T * kIdxHeads + i] * q_scale[(size_t)b * T * kIdxHeads + i];
-    if (tid < T) nvis[tid] = visible_entries(q_pos[b * T + tid], m, n_comp[b], Ncap);
+    if (warp == 1) ptx::tmem_alloc(&s.tmem_base, kTmemCols);
+    ptx::tc_fence_before();
     __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = s.tmem_base;
 
-    const int c = blockIdx.x * kKeysPerCta + tid;
-    if (c >= Ncap) return;
-    int nv_max = 0;
-    for (int t = 0; t < T; ++t) nv_max = max(nv_max, nvis[t]);
-    if (c >= nv_max) {
-        for (int t = 0; t < T; ++t) logits[((size_t)b * T + t) * Ncap + c] = -INFINITY;
-        return;
-    }
-    float kf[kIdxDim];
-    const uint4 *kp = reinterpret_cast<const uint4 *>(k_idx + ((size_t)b * Ncap + c) * kIdxDim);
-#pragma unroll
-    for (int v = 0; v < kIdxDim / 16; ++v) {
-        uint4 u = __ldg(kp + v);
-        uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float2 lo = e4m3x2_to_float2(static_cast<uint16_t>(w4[j] & 0xFFFF));
-            float2 hi = e4m3x2_to_float2(static_cast<uint16_t>(w4[j] >> 16));
-            kf[v * 16 + j * 4 + 0] = lo.x;
-            kf[v * 16 + j * 4 + 1] = lo.y;
-            kf[v * 16 + j * 4 + 2] = hi.x;
-            kf[v * 16 + j * 4 + 3] = hi.y;
+    // Walks this CTA's tiles in order; identical in every role.
+    auto tile_at = [&](long i, int &cached_b, int &cached_nv) {
+        TileInfo ti;
+        ti.b = (int)(i / n_tiles);
+        ti.c0 = (int)(i % n_tiles) * kTileKeys;
+        if (ti.b != cached_b) {
+            cached_b = ti.b;
+            cached_nv = seq_visible_max(q_pos, n_comp, ti.b, T, m, Ncap);
         }
-    }
-    const float sk = __ldg(k_scale + (size_t)b * Ncap + c);
-    for (int t = 0; t < T; ++t) {
-        float acc = 0.f;
-        for (int h = 0; h < kIdxHeads; ++h) {
-            const float4 *qrow = reinterpret_cast<const float4 *>(qf + (t * kIdxHeads + h) * kIdxDim);
-            float dot = 0.f;
-#pragma unroll
-            for (int d4 = 0; d4 < kIdxDim / 4; ++d4) {
-                float4 qv = qrow[d4];
-                dot = fmaf(qv.x, kf[d4 * 4 + 0], dot);
-                dot = fmaf(qv.y, kf[d4 * 4 + 1], dot);
-                dot = fmaf(qv.z, kf[d4 * 4 + 2], dot);
-                dot = fmaf(qv.w, kf[d4 * 4 + 3], dot);
+        ti.skip = ti.c0 >= cached_nv;
+        return ti;
+    };
+    auto fail = [&]() {
+        report_error(err, CSA_ERR_TIMEOUT);
+        *abort = 1;
+    };
+    // every lane of a warp waits; the outcome is made warp-uniform
+    auto wait = [&](uint64_t *bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort, kWaitLimitNs)) != 0;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int cb = -1, cnv = 0, active_b = -1;
+        uint32_t j = 0, u = 0;  // tiles loaded, query slots filled
+        const uint64_t policy = ptx::l2_policy_evict_first();
+        if (lane == 0) {
+            ptx::prefetch_tensormap(&kmap);
+            ptx::prefetch_tensormap(&qmap);
+        }
+        bool ok = true;
+        for (long i = t_begin; i < t_end && ok; ++i) {
+            const TileInfo ti = tile_at(i, cb, cnv);
+            if (ti.skip) continue;
+            if (ti.b != active_b) {
+                active_b = ti.b;
+                const int slot = u & 1;
+                if (!wait(&s.q_empty[slot], ((u >> 1) & 1) ^ 1)) { fail(); ok = false; break; }
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(&s.q_full[slot], IdxSmem<T>::kQBytes);
+                    ptx::tma_load_2d(s.q[slot], &qmap, &s.q_full[slot], 0, ti.b * N);
+                }
+                for (int h = lane; h < N; h += 32)
+                    s.ws[slot][h] = __ldg(w_idx + (size_t)ti.b * N + h) * __ldg(q_scale + (size_t)ti.b * N + h);
+                ptx::mbar_arrive(&s.q_full[slot]);
+                ++u;
             }
-            acc = fmaf(ws[t * kIdxHeads + h], fmaxf(dot, 0.f), acc);
+            const int st = j % kStages;
+            if (!wait(&s.empty[st], ((j / kStages) & 1) ^ 1)) { fail(); ok = false; break; }
+            if (lane == 0) {
+                ptx::mbar_arrive_expect_tx(&s.full[st], kTileBytes);
+                ptx::tma_load_2d_hint(s.keys[st], &kmap, &s.full[st], 0, ti.b * Ncap + ti.c0, policy);
+            }
+            __syncwarp();
+            ++j;
         }
-        logits[((size_t)b * T + t) * Ncap + c] = c < nvis[t] ? acc * sk : -INFINITY;
+        // drain: every issued copy has landed before the CTA may exit
+        for (uint32_t q = (j > kStages ? j - kStages : 0); q < j; ++q)
+            wait(&s.full[q % kStages], (q / kStages) & 1);
+        for (uint32_t q = (u > 2 ? u - 2 : 0); q < u; ++q)
+            wait(&s.q_full[q & 1], (q >> 1) & 1);
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        int cb = -1, cnv = 0, active_b = -1;
+        uint32_t j = 0, u = 0, a = 0;
+        bool ok = true;
+        for (long i = t_begin; i < t_end && ok; ++i) {
+            const TileInfo ti = tile_at(i, cb, cnv);
+            if (ti.skip) continue;
+            if (ti.b != active_b) {
+                if (active_b >= 0 && lane == 0) ptx::mma_commit(&s.q_empty[(u - 1) & 1]);
+                active_b = ti.b;
+                if (!wait(&s.q_full[u & 1], (u >> 1) & 1)) { fail(); ok = false; break; }
+                ++u;
+            }
+            const int st = j % kStages;
+            const int buf = a & 1;
+            if (!wait(&s.acc_empty[buf], ((a >> 1) & 1) ^ 1)) { fail(); ok = false; break; }
+            if (!wait(&s.full[st], (j / kStages) & 1)) { fail(); ok = false; break; }
+            ptx::tc_fence_after();
+            if (lane == 0) {
+                const uint32_t a_base = ptx::smem_u32(s.keys[st]);
+                const uint32_t b_base = ptx::smem_u32(s.q[(u - 1) & 1]);
+#pragma unroll
+                for (int kk = 0; kk < kIdxDim / 32; ++kk)
+                    ptx::mma_f8f6f4(tmem + buf * N, ptx::desc_kmajor_sw128(a_base + kk * 32),
+                                    ptx::desc_kmajor_sw128(b_base + kk * 32), kIdesc, kk > 0 ? 1u : 0u);
+                ptx::mma_commit(&s.empty[st]);
+                ptx::mma_commit(&s.acc_full[buf]);
+            }
+            __syncwarp();
+            ++j;
+            ++a;
+        }
+        if (lane == 0) {
+            if (active_b >= 0) ptx::mma_commit(&s.q_empty[(u - 1) & 1]);
+            ptx::mma_commit(&s.mma_done);
+        }
+        __syncwarp();
+        wait(&s.mma_done, 0);
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const int row = quarter * 32 + lane;
+        int cb = -1, cnv = 0, active_b = -1;
+        uint32_t u = 0, a = 0;
+        int nvis[T];
+        bool ok = true;
+        for (long i = t_begin; i < t_end && ok; ++i) {
+            const TileInfo ti = tile_at(i, cb, cnv);
+            const int c = ti.c0 + row;
+            float *lrow = logits + (size_t)ti.b * T * Ncap + c;
+            if (ti.skip) {
+                if (c < Ncap)
+                    for (int t = 0; t < T; ++t) lrow[(size_t)t * Ncap] = -INFINITY;
+                continue;
+            }
+            if (ti.b != active_b) {
+                if (active_b >= 0 && lane == 0) ptx::mbar_arrive(&s.q_empty[(u - 1) & 1]);
+                active_b = ti.b;
+                if (!wait(&s.q_full[u & 1], (u >> 1) & 1)) { fail(); ok = false; break; }
+                for (int t = 0; t < T; ++t)
+                    nvis[t] = visible_entries(__ldg(q_pos + ti.b * T + t), m, __ldg(n_comp + ti.b), Ncap);
+                ++u;
+            }
+            const int buf = a & 1;
+            if (!wait(&s.acc_full[buf], (a >> 1) & 1)) { fail(); ok = false; break; }
+            ptx::tc_fence_after();
+            const float *ws = s.ws[(u - 1) & 1];
+            const float sk = c < Ncap ? __ldg(k_scale + (size_t)ti.b * Ncap + c) : 0.f;
+            float acc[T];
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+                acc[t] = 0.f;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t r[32];
+                    ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + buf * N + t * kIdxHeads + half * 32, r);
+                    ptx::tmem_ld_wait();
+                    const float4 *w4 = reinterpret_cast<const float4 *>(ws + t * kIdxHeads + half * 32);
+#pragma unroll
+                    for (int h4 = 0; h4 < 8; ++h4) {
+                        const float4 wv = w4[h4];
+                        acc[t] = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f), acc[t]);
+                        acc[t] = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f), acc[t]);
+                        acc[t] = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f), acc[t]);
+                        acc[t] = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f), acc[t]);
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&s.acc_empty[buf]);
+            if (c < Ncap) {
+#pragma unroll
+                for (int t = 0; t < T; ++t) lrow[(size_t)t * Ncap] = c < nvis[t] ? acc[t] * sk : -INFINITY;
+            }
+            ++a;
+        }
+        if (ok && active_b >= 0 && lane == 0) ptx::mbar_arrive(&s.q_empty[(u - 1) & 1]);
     }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// A 2-D uint8 tensor map over rows of 128 bytes, box = 128 B x box_rows,
+// 128-byte swizzle (the layout the MMA descriptors above expect).
+bool make_rows128_map(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+template <int T>
+cudaError_t launch_t(const uint8_t *q_idx, const float *q_scale, const float *w_idx, const uint8_t *k_idx,
+                     const float *k_scale, const int32_t *q_pos, const int32_t *n_comp, int B, int Ncap, int m,
+                     float *logits, int *err, cudaStream_t stream) {
+    CUtensorMap kmap, qmap;
+    if (!make_rows128_map(&kmap, k_idx, (uint64_t)B * Ncap, kTileKeys) ||
+        !make_rows128_map(&qmap, q_idx, (uint64_t)B * T * kIdxHeads, T * kIdxHeads))
+        return cudaErrorInvalidValue;
+    const size_t smem = sizeof(IdxSmem<T>) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const long tiles = (long)B * ((Ncap + kTileKeys - 1) / kTileKeys);
+    const int grid = (int)std::min<long>(tiles, num_sms());
+    count_launch();
+    indexer_tc_kernel<T><<<grid, kThreads, smem, stream>>>(kmap, qmap, q_scale, w_idx, k_scale, q_pos, n_comp, B,
+                                                            Ncap, m, logits, err);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_indexer(const uint8_t *q_idx, const float *q_scale, const float *w_idx,
-                           const uint8_t *k_idx, const float *k_scale, const int32_t *q_pos,
-                           const int32_t *n_comp, int B, int T, int Ncap, int m, float *logits,
-                           cudaStream_t stream) {
-    size_t smem = sizeof(float) * (size_t)T * kIdxHeads * (kIdxDim + 1);
-    cudaError_t e = cudaFuncSetAttribute(indexer_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    dim3 grid((Ncap + kKeysPerCta - 1) / kKeysPerCta, B);
-    count_launch();
-    indexer_simt_kernel<<<grid, kKeysPerCta, smem, stream>>>(q_idx, q_scale, w_idx, k_idx, k_scale, q_pos,
-                                                              n_comp, T, Ncap, m, logits);
-    return cudaGetLastError();
+cudaError_t launch_indexer(const uint8_t *q_idx, const float *q_scale, const float *w_idx, const uint8_t *k_idx,
+                           const float *k_scale, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap,
+                           int m, float *logits, int *err, cudaStream_t stream) {
+    switch (T) {
+    case 1: return launch_t<1>(q_idx, q_scale, w_idx, k_idx, k_scale, q_pos, n_comp, B, Ncap, m, logits, err, stream);
+    case 2: return launch_t<2>(q_idx, q_scale, w_idx, k_idx, k_scale, q_pos, n_comp, B, Ncap, m, logits, err, stream);
+    case 3: return launch_t<3>(q_idx, q_scale, w_idx, k_idx, k_scale, q_pos, n_comp, B, Ncap, m, logits, err, stream);
+    case 4: return launch_t<4>(q_idx, q_scale, w_idx, k_idx, k_scale, q_pos, n_comp, B, Ncap, m, logits, err, stream);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace csa
