@@ -19,7 +19,7 @@ cudaError_t launch_gather(const csa_cache_desc &, const void *, int, int, const 
 size_t attention_workspace_bytes(int, int, int);
 cudaError_t launch_attention(const void *, const float *, float, const csa_cache_desc &, const void *, int, int,
                              const int32_t *, const int32_t *, const int32_t *, int, const int32_t *, int, int, int,
-                             bool, void *, float *, void *, size_t, int *, cudaStream_t);
+                             bool, int, void *, float *, void *, size_t, int *, cudaStream_t);
 }  // namespace csa
 
 namespace csa {
@@ -161,8 +161,8 @@ csa_status_t csa_sink_attention_decode(const void *q, const float *sink, float s
     if (need && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign)))
         return CSA_ERR_WORKSPACE;
     return cuda_status(launch_attention(q, sink, softmax_scale, comp, swa_ring, R, W, topk_idx, topk_cnt, nullptr, 1,
-                                        q_pos, B, T, k, false, out, lse, workspace, workspace_bytes,
-                                        device_error_word(), stream));
+                                        q_pos, B, T, k, false, k + CSA_MAX_SWA_WINDOW, out, lse, workspace,
+                                        workspace_bytes, device_error_word(), stream));
 }
 
 csa_status_t hca_sink_attention_decode(const void *q, const float *sink, float softmax_scale, csa_cache_desc comp,
@@ -177,8 +177,8 @@ csa_status_t hca_sink_attention_decode(const void *q, const float *sink, float s
     if (need && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign)))
         return CSA_ERR_WORKSPACE;
     return cuda_status(launch_attention(q, sink, softmax_scale, comp, swa_ring, R, W, nullptr, nullptr, n_comp, m_hca,
-                                        q_pos, B, T, 0, true, out, lse, workspace, workspace_bytes,
-                                        device_error_word(), stream));
+                                        q_pos, B, T, 0, true, comp.seq_capacity + CSA_MAX_SWA_WINDOW, out, lse,
+                                        workspace, workspace_bytes, device_error_word(), stream));
 }
 
 csa_status_t csa_decode_step(const uint8_t *q_idx, const float *q_idx_scale, const float *w_idx,

@@ -1,158 +1,608 @@
-// attention.cu -- sink-merged split-precision attention over the candidates
-// [top-k entries] ++ [SWA window] (CSA) or [all visible entries] ++ [SWA
-// window] (HCA) ("DSV4 Inference Kernel" README, Architecture; "DSV4 Audit",
-// sections A3 and B1).
+// attention.cu -- sink-merged split-precision attention on the tensor cores
+// over [top-k entries] ++ [SWA window] (CSA) or [all visible entries] ++
+// [SWA window] (HCA) ("DSV4 Inference Kernel" README, Architecture: one
+// 512-d latent per entry serves as key and value of all 128 heads, sink
+// weights merge the sparse and SWA terms; "DSV4 Audit", sections A3 and B1:
+// the FP8 nope dims are fed to attention without a BF16 copy in memory).
 //
-// The sink logit enters the running max and the denominator from the start
-// (m = sink, l = 1, o = 0), so the online softmax over the candidates ends at
-//   o = sum_j e^{z_j - M} x_j / (e^{sink - M} + sum_j e^{z_j - M}),
-//   lse = M + ln(den).
-// Candidates are read straight from the FP8/BF16 records, dequantised in
-// registers (nope code times its block multiplier; rope as BF16).
+// For head h over candidates j (x_j the dequantised latent):
+//   z_j = scale * q_h . x_j,  o_h = sum_j e^{z_j-M} x_j / (e^{sink_h-M} + sum_j e^{z_j-M}),
+//   lse_h = M + ln(den),  M = max(sink_h, max_j z_j).
+//
+// Work unit = (query token, candidate split), run by a cluster of two CTAs;
+// CTA rank r owns latent dims [256 r, 256 r + 256):
+//   * Q[:, half] (128 heads x 256 BF16) lives in TMEM and is the A operand of
+//     QK; each CTA computes the partial scores of its half for a chunk of 64
+//     candidates (tcgen05.mma kind::f16, M=128 heads, N=64, K=256) and the two
+//     partials are exchanged through distributed shared memory, so both CTAs
+//     hold identical full scores and run an identical softmax.
+//   * P (BF16) is written back into the score columns of TMEM and is the A
+//     operand of PV: O[:, half] += P X[:, half] (M=128, N=256, K=64); O stays
+//     in TMEM (256 fp32 columns) across chunks.
+//   * Candidate bytes are gathered straight from the FP8/BF16 caches (TMA bulk
+//     copies, block-table strided) and dequantised in shared memory to BF16
+//     (code x block multiplier); there is no dequantised copy in HBM.
+// Warps: 0 gather producer, 1 MMA issuer (and TMEM owner), 2-5 dequantise,
+// 6-9 softmax / exchange / epilogue (thread = head). The running max is
+// rescaled lazily (only when it grows by more than 2^8), in the log2 domain.
+// With one split per query the CTA pair writes the BF16 output and LSE; with
+// several, each split writes a normalised BF16 partial and (max, sum), and a
+// combine kernel folds the splits and the sink. Every wait is bounded.
+#include <cuda.h>
+
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace csa {
 
 namespace {
 
-constexpr int kHeadsPerCta = 8;  // one warp per head
+constexpr int kChunk = 64;                  // candidates per chunk
+constexpr int kHalf = 256;                  // latent dims per CTA
+constexpr int kSlot = 336;                  // staged bytes per candidate
+constexpr int kThreads = 320;               // 10 warps
+constexpr int kAtom = kChunk * 128;         // one 64-dim column block of X: 64 rows x 128 B
+constexpr int kXBytes = 4 * kAtom;          // 32 KB
+constexpr uint64_t kWaitNs = 1000000000ull; // 1 s per wait
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLazy = 8.f;                // rescale only when the max grows by > 2^8
 
-struct Lane16 {
-    float v[16];
+constexpr uint32_t kColQ = 0;    // 128 columns: Q half, BF16 pairs
+constexpr uint32_t kColO = 128;  // 256 columns: O half, fp32
+constexpr uint32_t kColS = 384;  // 2 x 64 columns: scores, then P (BF16 pairs) in the first 32
+constexpr uint32_t kTmemCols = 512;
+
+struct AttSmem {
+    alignas(1024) uint8_t x[2][kXBytes];        // dequantised candidates, 128-byte swizzle
+    alignas(1024) float4 recv[2][16 * kHeads];  // peer's partial scores: [16 float4][128 heads]
+    alignas(128) uint8_t stage[2][kChunk * kSlot];
+    uint64_t vmask[2], smask[2];
+    uint64_t stg_full[2], stg_empty[2], x_full[2], x_empty[2], s_full[2], p_full[2];
+    uint64_t xchg_full[2], xchg_free[2];
+    uint64_t o_done, q_ready, mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
 };
 
-// Latent dims owned by `lane`: lanes 0..27 hold nope dims [16 lane, 16 lane + 16),
-// lanes 28..31 hold rope dims [448 + 16 (lane-28), +16).
-__device__ __forceinline__ void load_latent(const uint8_t *rec, int lane, Lane16 &x) {
-    if (lane < 28) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(rec + lane * 16));
-        const float s = __ldg(reinterpret_cast<const float *>(rec + kScaleOffset) + (lane >> 3));
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float2 lo = e4m3x2_to_float2(static_cast<uint16_t>(w[j] & 0xFFFF));
-            float2 hi = e4m3x2_to_float2(static_cast<uint16_t>(w[j] >> 16));
-            x.v[4 * j + 0] = lo.x * s;
-            x.v[4 * j + 1] = lo.y * s;
-            x.v[4 * j + 2] = hi.x * s;
-            x.v[4 * j + 3] = hi.y * s;
-        }
+struct AttParams {
+    const __nv_bfloat16 *q;
+    const float *sink;
+    float scale_log2;  // softmax scale * log2(e)
+    CacheView comp;
+    const uint8_t *ring;
+    int R, W;
+    const int32_t *topk_idx, *topk_cnt, *n_comp, *q_pos;
+    int m_hca, hca, T, k, n_split;
+    __nv_bfloat16 *out;
+    float *lse;
+    __nv_bfloat16 *part_o;  // [rows, n_split, 128, 512] BF16 (n_split > 1)
+    float2 *part_ml;        // [rows, n_split, 128] (max, sum) in log2 units
+    int *err;
+};
+
+struct Unit {
+    int r, b, split, p, n_sel, j0, cb, ce, n_chunks;
+};
+
+__device__ __forceinline__ Unit make_unit(const AttParams &P) {
+    Unit u;
+    const int cluster = blockIdx.x >> 1;
+    u.r = cluster / P.n_split;
+    u.split = cluster % P.n_split;
+    u.b = u.r / P.T;
+    u.p = __ldg(P.q_pos + u.r);
+    if (P.hca) {
+        u.n_sel = visible_entries(u.p, P.m_hca, __ldg(P.n_comp + u.b), P.comp.seq_capacity);
     } else {
-        const uint4 *p = reinterpret_cast<const uint4 *>(rec + kRopeOffset + (lane - 28) * 32);
-        const uint4 a = __ldg(p), c = __ldg(p + 1);
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            x.v[2 * j + 0] = bf16_bits_to_float(static_cast<uint16_t>(w[j] & 0xFFFF));
-            x.v[2 * j + 1] = bf16_bits_to_float(static_cast<uint16_t>(w[j] >> 16));
-        }
+        const int c = __ldg(P.topk_cnt + u.r);
+        u.n_sel = c < 0 ? 0 : (c > P.k ? P.k : c);
     }
+    u.j0 = max(0, u.p - P.W + 1);
+    const int nswa = u.p >= 0 ? u.p - u.j0 + 1 : 0;
+    const int n = u.n_sel + nswa;
+    const int per = ((n + P.n_split - 1) / P.n_split + kChunk - 1) / kChunk * kChunk;
+    u.cb = min(n, u.split * per);
+    u.ce = min(n, u.cb + per);
+    u.n_chunks = (u.ce - u.cb + kChunk - 1) / kChunk;
+    return u;
 }
 
-__device__ __forceinline__ int lane_dim0(int lane) { return lane < 28 ? lane * 16 : kNope + (lane - 28) * 16; }
+// Record of candidate i of the unit's list, or nullptr (outside the cache).
+__device__ __forceinline__ const uint8_t *candidate(const AttParams &P, const Unit &u, int i) {
+    if (i < u.n_sel) {
+        const int c = P.hca ? i : __ldg(P.topk_idx + (size_t)u.r * P.k + i);
+        const int64_t rec = record_index(P.comp, u.b, c);
+        return rec < 0 ? nullptr : P.comp.base + rec * kRecBytes;
+    }
+    const int pos = u.j0 + (i - u.n_sel);
+    return P.ring + ((int64_t)u.b * P.R + pos % P.R) * kRecBytes;
+}
 
-__global__ void __launch_bounds__(kHeadsPerCta * 32)
-attention_simt_kernel(const __nv_bfloat16 *__restrict__ q, const float *__restrict__ sink, float scale,
-                      CacheView comp, const uint8_t *__restrict__ ring, int R, int W,
-                      const int32_t *__restrict__ topk_idx, const int32_t *__restrict__ topk_cnt,
-                      const int32_t *__restrict__ n_comp, int m_hca, const int32_t *__restrict__ q_pos,
-                      int T, int k, int hca, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse,
-                      int *err) {
-    const int r = blockIdx.y;
-    const int b = r / T;
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// 8 E4M3 codes (two 32-bit words) times a multiplier -> 8 BF16 values (uint4).
+__device__ __forceinline__ uint4 dequant8(uint32_t w0, uint32_t w1, float s) {
+    uint32_t out[4];
+    const uint32_t w[2] = {w0, w1};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float2 a = e4m3x2_to_float2(static_cast<uint16_t>(w[i] & 0xFFFFu));
+        const float2 c = e4m3x2_to_float2(static_cast<uint16_t>(w[i] >> 16));
+        out[2 * i] = bf16x2_bits(a.x * s, a.y * s);
+        out[2 * i + 1] = bf16x2_bits(c.x * s, c.y * s);
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+attention_tc_kernel(const AttParams P) {
+    extern __shared__ uint8_t smem_raw[];
+    AttSmem &s = *reinterpret_cast<AttSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = blockIdx.x * kHeadsPerCta + warp;
-    const int d0 = lane_dim0(lane);
-    const int p = q_pos[r];
+    const uint32_t rank = ptx::cluster_ctarank();
+    const uint32_t peer = rank ^ 1u;
+    volatile int *abort = &s.abort_flag;
+    const Unit u = make_unit(P);
 
-    int n_sel;
-    if (hca) {
-        n_sel = visible_entries(p, m_hca, n_comp[b], comp.seq_capacity);
-    } else {
-        n_sel = topk_cnt[r];
-        if (n_sel < 0 || n_sel > k) {
-            if (lane == 0) report_error(err, CSA_ERR_BAD_INDEX);
-            n_sel = n_sel < 0 ? 0 : k;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&s.stg_full[i], 32);
+            ptx::mbar_init(&s.stg_empty[i], 4);
+            ptx::mbar_init(&s.x_full[i], 4);
+            ptx::mbar_init(&s.x_empty[i], 1);
+            ptx::mbar_init(&s.s_full[i], 1);
+            ptx::mbar_init(&s.p_full[i], 4);
+            ptx::mbar_init(&s.xchg_full[i], 128);
+            ptx::mbar_init(&s.xchg_free[i], 128);
         }
+        ptx::mbar_init(&s.o_done, 1);
+        ptx::mbar_init(&s.q_ready, 4);
+        ptx::mbar_init(&s.mma_done, 1);
+        s.abort_flag = 0;
+        ptx::fence_mbar_init();
     }
-    if (p < 0 && lane == 0) report_error(err, CSA_ERR_BAD_INDEX);
-    const int j0 = max(0, p - W + 1);
-    const int nswa = p >= 0 ? p - j0 + 1 : 0;
+    if (warp == 1) ptx::tmem_alloc(&s.tmem_base, kTmemCols);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::cluster_sync();  // the peer's barriers exist before anyone signals them
+    ptx::tc_fence_after();
+    const uint32_t tmem = s.tmem_base;
 
-    float qv[16];
-    {
-        const uint4 *qp = reinterpret_cast<const uint4 *>(q + ((size_t)r * kHeads + h) * kDim + d0);
-        const uint4 a = __ldg(qp), c = __ldg(qp + 1);
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+    auto fail = [&]() {
+        report_error(P.err, CSA_ERR_TIMEOUT);
+        *abort = 1;
+    };
+    auto wait = [&](uint64_t *bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort, kWaitNs)) != 0;
+    };
+    auto wait_cluster = [&](uint64_t *bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, ptx::mbar_wait_cluster(bar, parity, abort, kWaitNs)) != 0;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ gather producer
+        int j = 0;
+        bool ok = true;
+        for (; j < u.n_chunks && ok; ++j) {
+            const int jb = j & 1;
+            if (!wait(&s.stg_empty[jb], ((j >> 1) & 1) ^ 1)) { fail(); ok = false; break; }
+            bool valid[2];
+            const uint8_t *rec[2];
+            uint32_t bytes = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            qv[2 * j + 0] = bf16_bits_to_float(static_cast<uint16_t>(w[j] & 0xFFFF));
-            qv[2 * j + 1] = bf16_bits_to_float(static_cast<uint16_t>(w[j] >> 16));
-        }
-    }
-
-    const float sk = sink[h];
-    float mrun = sk;                          // running max, starts at the sink logit
-    float l = (sk == -INFINITY) ? 0.f : 1.f;  // e^{sink - m}
-    float o[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) o[i] = 0.f;
-
-    const int n = n_sel + nswa;
-    for (int j = 0; j < n; ++j) {
-        const uint8_t *rec;
-        if (j < n_sel) {
-            const int c = hca ? j : __ldg(topk_idx + (size_t)r * k + j);
-            const int64_t ri = record_index(comp, b, c);
-            if (ri < 0) {
-                if (lane == 0) report_error(err, CSA_ERR_BAD_INDEX);
-                continue;
+            for (int e = 0; e < 2; ++e) {
+                const int ci = 2 * lane + e;
+                const int i = u.cb + j * kChunk + ci;
+                rec[e] = i < u.ce ? candidate(P, u, i) : nullptr;
+                valid[e] = rec[e] != nullptr;
+                if (i < u.ce && !valid[e] && rank == 0) report_error(P.err, CSA_ERR_BAD_INDEX);
+                bytes += valid[e] ? (rank == 0 ? 272u : 336u) : 0u;
             }
-            rec = comp.base + ri * kRecBytes;
-        } else {
-            const int pos = j0 + (j - n_sel);
-            rec = ring + ((int64_t)b * R + pos % R) * kRecBytes;
+            if (bytes) ptx::mbar_expect_tx(&s.stg_full[jb], bytes);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                if (!valid[e]) continue;
+                uint8_t *dst = s.stage[jb] + (2 * lane + e) * kSlot;
+                if (rank == 0) {
+                    ptx::bulk_g2s(dst, rec[e], 256, &s.stg_full[jb]);
+                    ptx::bulk_g2s(dst + 256, rec[e] + kScaleOffset, 16, &s.stg_full[jb]);
+                } else {
+                    ptx::bulk_g2s(dst, rec[e] + 256, 336, &s.stg_full[jb]);
+                }
+            }
+            const uint32_t m0 = __ballot_sync(0xffffffffu, valid[0]);
+            const uint32_t m1 = __ballot_sync(0xffffffffu, valid[1]);
+            if (lane == 0) {
+                uint64_t mask = 0;
+                for (int L = 0; L < 32; ++L)
+                    mask |= (uint64_t)((m0 >> L) & 1u) << (2 * L) | (uint64_t)((m1 >> L) & 1u) << (2 * L + 1);
+                s.vmask[jb] = mask;
+            }
+            __syncwarp();
+            ptx::mbar_arrive(&s.stg_full[jb]);
         }
-        Lane16 x;
-        load_latent(rec, lane, x);
-        float dot = 0.f;
+        // drain: every issued copy has landed before the CTA may exit
+        for (int q = (j > 2 ? j - 2 : 0); q < j; ++q) wait(&s.stg_full[q & 1], (q >> 1) & 1);
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t kIdescQK = ptx::idesc_f32acc(1, 1, 128, kChunk);
+        constexpr uint32_t kIdescPV = ptx::idesc_f32acc(1, 1, 128, kHalf, 1);
+        bool ok = u.n_chunks == 0 || wait(&s.q_ready, 0);
+        if (!ok) fail();
+        auto issue_pv = [&](int jp) -> bool {
+            const int pb = jp & 1;
+            if (!wait(&s.p_full[pb], (jp >> 1) & 1)) return false;
+            ptx::tc_fence_after();
+            if (lane == 0) {
+                const uint32_t xb = ptx::smem_u32(s.x[pb]);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) dot = fmaf(qv[i], x.v[i], dot);
+                for (int kk = 0; kk < kChunk / 16; ++kk)
+                    ptx::mma_f16_ts(tmem + kColO, tmem + kColS + pb * kChunk + kk * 8,
+                                    ptx::desc_mnmajor_sw128(xb + kk * 2048, kAtom, 1024), kIdescPV,
+                                    (jp > 0 || kk > 0) ? 1u : 0u);
+                ptx::mma_commit(&s.x_empty[pb]);
+                ptx::mma_commit(&s.o_done);
+            }
+            __syncwarp();
+            return true;
+        };
+        for (int j = 0; j < u.n_chunks && ok; ++j) {
+            const int jb = j & 1;
+            if (!wait(&s.x_full[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
+            ptx::tc_fence_after();
+            if (lane == 0) {
+                const uint32_t xb = ptx::smem_u32(s.x[jb]);
 #pragma unroll
-        for (int o2 = 16; o2 > 0; o2 >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o2);
-        const float z = dot * scale;
-        const float mnew = fmaxf(mrun, z);
-        const float corr = __expf(mrun - mnew);
-        const float pj = __expf(z - mnew);
-        l = l * corr + pj;
+                for (int kk = 0; kk < kHalf / 16; ++kk)
+                    ptx::mma_f16_ts(tmem + kColS + jb * kChunk, tmem + kColQ + kk * 8,
+                                    ptx::desc_kmajor_sw128(xb + (kk >> 2) * kAtom + (kk & 3) * 32), kIdescQK,
+                                    kk > 0 ? 1u : 0u);
+                ptx::mma_commit(&s.s_full[jb]);
+            }
+            __syncwarp();
+            if (j > 0 && !issue_pv(j - 1)) { fail(); ok = false; break; }
+        }
+        if (ok && u.n_chunks > 0 && !issue_pv(u.n_chunks - 1)) fail();
+        if (lane == 0) ptx::mma_commit(&s.mma_done);
+        __syncwarp();
+        wait(&s.mma_done, 0);
+    } else if (warp < 6) {
+        // ------------------------------------------------------------ dequantise
+        const int ct = threadIdx.x - 64;  // 0..127
+        const int ci = ct >> 1;           // candidate row of the chunk
+        const int half = ct & 1;          // local dims [128 half, 128 half + 128)
+        bool ok = true;
+        for (int j = 0; j < u.n_chunks && ok; ++j) {
+            const int jb = j & 1;
+            if (!wait(&s.stg_full[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
+            if (!wait(&s.x_empty[jb], ((j >> 1) & 1) ^ 1)) { fail(); ok = false; break; }
+            const uint64_t mask = s.vmask[jb];
+            const bool valid = (mask >> ci) & 1ull;
+            const uint8_t *slot = s.stage[jb] + ci * kSlot;
+            uint8_t *xrow = s.x[jb] + ci * 128;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) o[i] = fmaf(o[i], corr, pj * x.v[i]);
-        mrun = mnew;
+            for (int aa = 0; aa < 2; ++aa) {
+                const int atom = 2 * half + aa;  // local dims [64 atom, 64 atom + 64)
+                uint8_t *xa = xrow + atom * kAtom;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    const int d = atom * 64 + cc * 8;  // first local dim of this 16-byte chunk
+                    uint4 v = make_uint4(0, 0, 0, 0);
+                    if (valid) {
+                        if (rank == 1 && d >= 192) {
+                            v = *reinterpret_cast<const uint4 *>(slot + 192 + (d - 192) * 2);  // rope, BF16
+                        } else {
+                            const uint2 codes = *reinterpret_cast<const uint2 *>(slot + d);
+                            const int blk = (rank == 0 ? d : 256 + d) >> 7;
+                            const float sc = *reinterpret_cast<const float *>(slot + (rank == 0 ? 256 : 320) + 4 * blk);
+                            v = dequant8(codes.x, codes.y, sc);
+                        }
+                    }
+                    *reinterpret_cast<uint4 *>(xa + ((cc ^ (ci & 7)) << 4)) = v;
+                }
+            }
+            ptx::fence_proxy_async_smem();  // generic-proxy stores -> MMA (async proxy) reads
+            if (ct == 0) s.smask[jb] = mask;
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(&s.stg_empty[jb]);
+                ptx::mbar_arrive(&s.x_full[jb]);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax / exchange / epilogue
+        const int quarter = warp & 3;
+        const int h = quarter * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int r = u.r;
+        bool ok = true;
+        // Q half -> TMEM (BF16 pairs, lane = head)
+        if (u.n_chunks > 0) {
+            const uint4 *qg = reinterpret_cast<const uint4 *>(P.q + ((size_t)r * kHeads + h) * kDim + rank * kHalf);
+#pragma unroll
+            for (int piece = 0; piece < 4; ++piece) {
+                uint32_t regs[32];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    const uint4 w4 = __ldg(qg + piece * 8 + v);
+                    regs[4 * v] = w4.x;
+                    regs[4 * v + 1] = w4.y;
+                    regs[4 * v + 2] = w4.z;
+                    regs[4 * v + 3] = w4.w;
+                }
+                ptx::tmem_st32(lane_base + kColQ + piece * 32, regs);
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&s.q_ready);
+        }
+        const uint32_t recv_peer[2] = {ptx::mapa(ptx::smem_u32(s.recv[0]), peer),
+                                       ptx::mapa(ptx::smem_u32(s.recv[1]), peer)};
+        const uint32_t full_peer[2] = {ptx::mapa(ptx::smem_u32(&s.xchg_full[0]), peer),
+                                       ptx::mapa(ptx::smem_u32(&s.xchg_full[1]), peer)};
+        const uint32_t free_peer[2] = {ptx::mapa(ptx::smem_u32(&s.xchg_free[0]), peer),
+                                       ptx::mapa(ptx::smem_u32(&s.xchg_free[1]), peer)};
+        float m = -INFINITY, l = 0.f;  // running max and sum, log2 domain, sink not included
+        for (int j = 0; j < u.n_chunks && ok; ++j) {
+            const int jb = j & 1;
+            if (!wait(&s.s_full[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
+            ptx::tc_fence_after();
+            uint32_t sa[32], sb[32];
+            ptx::tmem_ld32(lane_base + kColS + jb * kChunk, sa);
+            ptx::tmem_ld32(lane_base + kColS + jb * kChunk + 32, sb);
+            ptx::tmem_ld_wait();
+            // exchange partial scores with the peer CTA
+            if (j >= 2 && !wait_cluster(&s.xchg_free[jb], ((j - 2) >> 1) & 1)) { fail(); ok = false; break; }
+#pragma unroll
+            for (int cq = 0; cq < 8; ++cq) {
+                ptx::st_cluster_v4(recv_peer[jb] + (uint32_t)((cq * kHeads + h) * 16),
+                                   make_float4(__uint_as_float(sa[4 * cq]), __uint_as_float(sa[4 * cq + 1]),
+                                               __uint_as_float(sa[4 * cq + 2]), __uint_as_float(sa[4 * cq + 3])));
+                ptx::st_cluster_v4(recv_peer[jb] + (uint32_t)(((8 + cq) * kHeads + h) * 16),
+                                   make_float4(__uint_as_float(sb[4 * cq]), __uint_as_float(sb[4 * cq + 1]),
+                                               __uint_as_float(sb[4 * cq + 2]), __uint_as_float(sb[4 * cq + 3])));
+            }
+            ptx::mbar_arrive_remote(full_peer[jb]);
+            if (!wait_cluster(&s.xchg_full[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
+            float z[kChunk];
+#pragma unroll
+            for (int cq = 0; cq < 16; ++cq) {
+                const float4 pv = s.recv[jb][cq * kHeads + h];
+                const uint32_t *own = cq < 8 ? &sa[4 * cq] : &sb[4 * (cq - 8)];
+                z[4 * cq + 0] = __uint_as_float(own[0]) + pv.x;
+                z[4 * cq + 1] = __uint_as_float(own[1]) + pv.y;
+                z[4 * cq + 2] = __uint_as_float(own[2]) + pv.z;
+                z[4 * cq + 3] = __uint_as_float(own[3]) + pv.w;
+            }
+            ptx::mbar_arrive_remote(free_peer[jb]);
+            if (!wait(&s.x_full[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
+            const uint64_t mask = s.smask[jb];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kChunk; ++c) {
+                z[c] = ((mask >> c) & 1ull) ? z[c] * P.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, z[c]);
+            }
+            if (mx > m + kLazy || (m == -INFINITY && mx > -INFINITY)) {
+                const float alpha = exp2f(m - mx);  // 0 when m = -inf
+                if (j > 0) {
+                    // O holds PV of chunks < j: wait for the last one, then rescale in place
+                    if (!wait(&s.o_done, (j - 1) & 1)) { fail(); ok = false; break; }
+                    ptx::tc_fence_after();
+#pragma unroll 1
+                    for (int piece = 0; piece < kHalf / 32; ++piece) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32(lane_base + kColO + piece * 32, o);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        ptx::tmem_st32(lane_base + kColO + piece * 32, o);
+                    }
+                    ptx::tmem_st_wait();
+                }
+                l *= alpha;
+                m = mx;
+            }
+            uint32_t pk[32];
+            float psum = 0.f;
+            const float mref = (m == -INFINITY) ? 0.f : m;  // every z is -inf while m is
+#pragma unroll
+            for (int c2 = 0; c2 < kChunk / 2; ++c2) {
+                const float p0 = exp2f(z[2 * c2] - mref), p1 = exp2f(z[2 * c2 + 1] - mref);
+                psum += p0 + p1;
+                pk[c2] = bf16x2_bits(p0, p1);
+            }
+            l += psum;
+            ptx::tmem_st32(lane_base + kColS + jb * kChunk, pk);
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&s.p_full[jb]);
+        }
+        // ---------------- epilogue: O half (and LSE) out
+        if (ok && u.n_chunks > 0) {
+            if (!wait(&s.o_done, (u.n_chunks - 1) & 1)) { fail(); ok = false; }
+            ptx::tc_fence_after();
+        }
+        if (ok) {
+            float factor, lse_out = 0.f;
+            const float2 ml = make_float2(m, l);
+            if (P.n_split == 1) {
+                const float sk = __ldg(P.sink + h) * kLog2e;
+                const float M = fmaxf(sk, m);
+                const float es = (sk == -INFINITY) ? 0.f : exp2f(sk - M);
+                const float eo = (m == -INFINITY) ? 0.f : exp2f(m - M);
+                const float den = es + l * eo;
+                factor = den > 0.f ? eo / den : 0.f;
+                lse_out = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
+            } else {
+                factor = l > 0.f ? 1.f / l : 0.f;
+            }
+            __nv_bfloat16 *dst = (P.n_split == 1)
+                                     ? P.out + ((size_t)r * kHeads + h) * kDim + rank * kHalf
+                                     : P.part_o + (((size_t)r * P.n_split + u.split) * kHeads + h) * kDim + rank * kHalf;
+#pragma unroll 1
+            for (int piece = 0; piece < kHalf / 32; ++piece) {
+                uint32_t o[32];
+                if (u.n_chunks > 0) {
+                    ptx::tmem_ld32(lane_base + kColO + piece * 32, o);
+                    ptx::tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst + piece * 32);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    d4[v] = make_uint4(bf16x2_bits(__uint_as_float(o[8 * v + 0]) * factor, __uint_as_float(o[8 * v + 1]) * factor),
+                                       bf16x2_bits(__uint_as_float(o[8 * v + 2]) * factor, __uint_as_float(o[8 * v + 3]) * factor),
+                                       bf16x2_bits(__uint_as_float(o[8 * v + 4]) * factor, __uint_as_float(o[8 * v + 5]) * factor),
+                                       bf16x2_bits(__uint_as_float(o[8 * v + 6]) * factor, __uint_as_float(o[8 * v + 7]) * factor));
+            }
+            if (rank == 0) {
+                if (P.n_split == 1)
+                    P.lse[(size_t)r * kHeads + h] = lse_out;
+                else
+                    P.part_ml[((size_t)r * P.n_split + u.split) * kHeads + h] = ml;
+            }
+        }
     }
 
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    __nv_bfloat16 ob[16];
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::cluster_sync();  // no remote access to this CTA's shared memory after this point
+    ptx::tc_fence_after();
+    if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+// Folds the per-split normalised partials and the sink:
+//   M = max(sink, m_s), den = e^{sink-M} + sum_s l_s e^{m_s-M},
+//   out = sum_s l_s e^{m_s-M} o_s / den, lse = M + ln den   (log2 domain inside).
+__global__ void __launch_bounds__(256)
+attention_combine_kernel(const __nv_bfloat16 *__restrict__ part_o, const float2 *__restrict__ part_ml,
+                         const float *__restrict__ sink, int n_split, __nv_bfloat16 *__restrict__ out,
+                         float *__restrict__ lse) {
+    const int r = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.x * 8 + warp;
+    const float sk = __ldg(sink + h) * kLog2e;
+    float M = sk;
+    for (int sp = 0; sp < n_split; ++sp) {
+        const float2 ml = part_ml[((size_t)r * n_split + sp) * kHeads + h];
+        if (ml.y > 0.f) M = fmaxf(M, ml.x);
+    }
+    float den = (sk == -INFINITY) ? 0.f : exp2f(sk - M);
+    float acc[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) ob[i] = __float2bfloat16_rn(o[i] * inv);
-    uint4 *op = reinterpret_cast<uint4 *>(out + ((size_t)r * kHeads + h) * kDim + d0);
-    op[0] = *reinterpret_cast<const uint4 *>(&ob[0]);
-    op[1] = *reinterpret_cast<const uint4 *>(&ob[8]);
-    if (lane == 0) lse[(size_t)r * kHeads + h] = l > 0.f ? mrun + logf(l) : sk;
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+    for (int sp = 0; sp < n_split; ++sp) {
+        const float2 ml = part_ml[((size_t)r * n_split + sp) * kHeads + h];
+        if (!(ml.y > 0.f)) continue;
+        const float w = ml.y * exp2f(ml.x - M);
+        den += w;
+        const uint4 *src = reinterpret_cast<const uint4 *>(part_o + (((size_t)r * n_split + sp) * kHeads + h) * kDim) + lane * 2;
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+            const uint4 x = src[v];
+            const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[8 * v + 2 * i] = fmaf(w, bf16_bits_to_float(static_cast<uint16_t>(wv[i] & 0xFFFFu)), acc[8 * v + 2 * i]);
+                acc[8 * v + 2 * i + 1] = fmaf(w, bf16_bits_to_float(static_cast<uint16_t>(wv[i] >> 16)), acc[8 * v + 2 * i + 1]);
+            }
+        }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)r * kHeads + h) * kDim) + lane * 2;
+#pragma unroll
+    for (int v = 0; v < 2; ++v)
+        dst[v] = make_uint4(bf16x2_bits(acc[8 * v + 0] * inv, acc[8 * v + 1] * inv),
+                            bf16x2_bits(acc[8 * v + 2] * inv, acc[8 * v + 3] * inv),
+                            bf16x2_bits(acc[8 * v + 4] * inv, acc[8 * v + 5] * inv),
+                            bf16x2_bits(acc[8 * v + 6] * inv, acc[8 * v + 7] * inv));
+    if (lane == 0) lse[(size_t)r * kHeads + h] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+// Splits per query so that about one CTA pair per two SMs is busy.
+int choose_splits(int rows, int max_candidates) {
+    const int chunks = (max_candidates + kChunk - 1) / kChunk;
+    const int target = sm_count() / 2;
+    int n = target / (rows > 0 ? rows : 1);
+    if (n > chunks) n = chunks;
+    return n < 1 ? 1 : n;
+}
+
+size_t split_bytes(int rows, int n_split) {
+    if (n_split <= 1) return 0;
+    const size_t po = (size_t)rows * n_split * kHeads * kDim * sizeof(__nv_bfloat16);
+    return (po + 255) / 256 * 256 + (size_t)rows * n_split * kHeads * sizeof(float2);
 }
 
 }  // namespace
 
-size_t attention_workspace_bytes(int, int, int) { return 0; }
+size_t attention_workspace_bytes(int B, int T, int max_candidates) {
+    const int rows = B * T;
+    return split_bytes(rows, choose_splits(rows, max_candidates));
+}
 
 cudaError_t launch_attention(const void *q, const float *sink, float scale, const csa_cache_desc &comp,
                              const void *ring, int R, int W, const int32_t *topk_idx, const int32_t *topk_cnt,
                              const int32_t *n_comp, int m_hca, const int32_t *q_pos, int B, int T, int k, bool hca,
-                             void *out, float *lse, void *, size_t, int *err, cudaStream_t stream) {
-    dim3 grid(kHeads / kHeadsPerCta, B * T);
+                             int max_candidates, void *out, float *lse, void *ws, size_t ws_bytes, int *err,
+                             cudaStream_t stream) {
+    const int rows = B * T;
+    const int n_split = choose_splits(rows, max_candidates);
+    AttParams P;
+    P.q = static_cast<const __nv_bfloat16 *>(q);
+    P.sink = sink;
+    P.scale_log2 = scale * kLog2e;
+    P.comp = make_view(comp);
+    P.ring = static_cast<const uint8_t *>(ring);
+    P.R = R;
+    P.W = W;
+    P.topk_idx = topk_idx;
+    P.topk_cnt = topk_cnt;
+    P.n_comp = n_comp;
+    P.q_pos = q_pos;
+    P.m_hca = m_hca;
+    P.hca = hca ? 1 : 0;
+    P.T = T;
+    P.k = k;
+    P.n_split = n_split;
+    P.out = static_cast<__nv_bfloat16 *>(out);
+    P.lse = lse;
+    P.part_o = nullptr;
+    P.part_ml = nullptr;
+    P.err = err;
+    if (n_split > 1) {
+        const size_t need = split_bytes(rows, n_split);
+        if (!ws || ws_bytes < need) return cudaErrorInvalidValue;
+        const size_t po = (size_t)rows * n_split * kHeads * kDim * sizeof(__nv_bfloat16);
+        P.part_o = static_cast<__nv_bfloat16 *>(ws);
+        P.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(ws) + (po + 255) / 256 * 256);
+    }
+    const size_t smem = sizeof(AttSmem) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     count_launch();
-    attention_simt_kernel<<<grid, kHeadsPerCta * 32, 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(q), sink, scale, make_view(comp), static_cast<const uint8_t *>(ring), R, W,
-        topk_idx, topk_cnt, n_comp, m_hca, q_pos, T, k, hca ? 1 : 0, static_cast<__nv_bfloat16 *>(out), lse, err);
+    attention_tc_kernel<<<2 * rows * n_split, kThreads, smem, stream>>>(P);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || n_split == 1) return e;
+    count_launch();
+    attention_combine_kernel<<<dim3(kHeads / 8, rows), 256, 0, stream>>>(P.part_o, P.part_ml, sink, n_split,
+                                                                         P.out, lse);
     return cudaGetLastError();
 }
 

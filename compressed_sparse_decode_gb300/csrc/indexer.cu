@@ -209,11 +209,23 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const int row = quarter * 32 + lane;
         int cb = -1, cnv = 0, active_b = -1;
+        int pb = -1, pnv = 0;  // visibility cache of the prefetch walk
         uint32_t u = 0, a = 0;
         int nvis[T];
+        // key scales are fetched one tile ahead so that their HBM latency
+        // overlaps the current tile instead of stalling it
+        auto fetch_scale = [&](long i) -> float {
+            if (i >= t_end) return 0.f;
+            const TileInfo ti = tile_at(i, pb, pnv);
+            const int c = ti.c0 + row;
+            return (!ti.skip && c < Ncap) ? __ldg(k_scale + (size_t)ti.b * Ncap + c) : 0.f;
+        };
+        float sk_next = fetch_scale(t_begin);
         bool ok = true;
         for (long i = t_begin; i < t_end && ok; ++i) {
             const TileInfo ti = tile_at(i, cb, cnv);
+            const float sk = sk_next;
+            sk_next = fetch_scale(i + 1);
             const int c = ti.c0 + row;
             float *lrow = logits + (size_t)ti.b * T * Ncap + c;
             if (ti.skip) {
@@ -233,26 +245,29 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             if (!wait(&s.acc_full[buf], (a >> 1) & 1)) { fail(); ok = false; break; }
             ptx::tc_fence_after();
             const float *ws = s.ws[(u - 1) & 1];
-            const float sk = c < Ncap ? __ldg(k_scale + (size_t)ti.b * Ncap + c) : 0.f;
             float acc[T];
 #pragma unroll
             for (int t = 0; t < T; ++t) {
-                acc[t] = 0.f;
+                uint32_t r0[32], r1[32];
+                const uint32_t col = tmem + ((uint32_t)(quarter * 32) << 16) + buf * N + t * kIdxHeads;
+                ptx::tmem_ld32(col, r0);
+                ptx::tmem_ld32(col + 32, r1);
+                ptx::tmem_ld_wait();
+                const float4 *w4 = reinterpret_cast<const float4 *>(ws + t * kIdxHeads);
+                float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t r[32];
-                    ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + buf * N + t * kIdxHeads + half * 32, r);
-                    ptx::tmem_ld_wait();
-                    const float4 *w4 = reinterpret_cast<const float4 *>(ws + t * kIdxHeads + half * 32);
-#pragma unroll
-                    for (int h4 = 0; h4 < 8; ++h4) {
-                        const float4 wv = w4[h4];
-                        acc[t] = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f), acc[t]);
-                        acc[t] = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f), acc[t]);
-                        acc[t] = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f), acc[t]);
-                        acc[t] = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f), acc[t]);
-                    }
+                for (int h4 = 0; h4 < 8; ++h4) {
+                    const float4 wa = w4[h4], wb = w4[8 + h4];
+                    s0 = fmaf(wa.x, fmaxf(__uint_as_float(r0[4 * h4 + 0]), 0.f), s0);
+                    s0 = fmaf(wa.y, fmaxf(__uint_as_float(r0[4 * h4 + 1]), 0.f), s0);
+                    s0 = fmaf(wa.z, fmaxf(__uint_as_float(r0[4 * h4 + 2]), 0.f), s0);
+                    s0 = fmaf(wa.w, fmaxf(__uint_as_float(r0[4 * h4 + 3]), 0.f), s0);
+                    s1 = fmaf(wb.x, fmaxf(__uint_as_float(r1[4 * h4 + 0]), 0.f), s1);
+                    s1 = fmaf(wb.y, fmaxf(__uint_as_float(r1[4 * h4 + 1]), 0.f), s1);
+                    s1 = fmaf(wb.z, fmaxf(__uint_as_float(r1[4 * h4 + 2]), 0.f), s1);
+                    s1 = fmaf(wb.w, fmaxf(__uint_as_float(r1[4 * h4 + 3]), 0.f), s1);
                 }
+                acc[t] = s0 + s1;
             }
             ptx::tc_fence_before();
             __syncwarp();
