@@ -18,8 +18,13 @@ the same seeded inputs). Tolerances, and where they come from:
 * Gather: byte-exact.
 * Attention output (BF16) vs the oracle's fp64 on the GPU's own selected set:
   per head cosine >= 0.999 and max_i |gpu - oracle| / max_i |oracle| <= 2e-2
-  (the stated tolerances, read per head). LSE: |gpu - oracle| <= 2e-3
-  absolute, from the fp32 online softmax and the BF16-rounded latent.
+  (the stated tolerances, read per head).
+* LSE (no stated tolerance; derived): the tensor-core path rounds each
+  dequantised latent element to BF16 (relative error <= 2^-9) and keeps q
+  exact, so each score z_j = scale q.x_j moves by at most
+  B_j = scale * 2^-9 * sum_d |q_d| |x_jd| (fp32 accumulation adds < 1e-5 of
+  that). LSE = ln sum_j e^{z_j} is 1-Lipschitz in the max-norm of the scores,
+  hence |gpu - oracle| <= max_j B_j + 1e-5 (1 + |lse|) per head.
 """
 from __future__ import annotations
 
@@ -104,8 +109,43 @@ def check_topk_band(gpu_idx, gpu_cnt, ora_scores, ora_idx, ora_cnt, k: int, what
     return swaps
 
 
-def check_attention(gpu_out: np.ndarray, gpu_lse: np.ndarray, ora_out: np.ndarray, ora_lse: np.ndarray, what: str):
-    """gpu_out/ora_out [rows, H, D]; returns (min cosine, max rel err, max lse err)."""
+def lse_bound(q_bits: np.ndarray, records: np.ndarray, scale: float) -> np.ndarray:
+    """max_j B_j per head for one query: q_bits [H, D] bf16 bits, records
+    [n, 592] candidate records (library casts for the dequantisation)."""
+    from _lib_refs import bf16_to_f64, dequant_records
+    if records.shape[0] == 0:
+        return np.zeros(q_bits.shape[0])
+    X = dequant_records(records, 448, 64, 128).abs()
+    Q = bf16_to_f64(np.ascontiguousarray(q_bits)).abs()
+    return (scale * 2.0 ** -9 * (Q @ X.T).max(dim=1).values).numpy()
+
+
+def candidate_records(x, r: int, sel) -> np.ndarray:
+    """Candidate records of flat query row r: comp entries ``sel`` then the SWA
+    window (numpy indexing of the cache arrays)."""
+    b, t = divmod(int(r), x.wl.T)
+    comp = x.comp.cpu().numpy()
+    sel = np.asarray(sel, dtype=np.int64)
+    if x.block_table is None:
+        rec_idx = b * x.seq_stride + sel
+    else:
+        bt = x.block_table.cpu().numpy()
+        rec_idx = bt[b, sel // x.page_records].astype(np.int64) * x.page_records + sel % x.page_records
+    p = int(x.q_pos.cpu().numpy()[b, t])
+    R = x.ring.shape[1]
+    win = [j % R for j in range(max(0, p - x.wl.W + 1), p + 1)]
+    return np.concatenate([comp[rec_idx], x.ring.cpu().numpy()[b, win]], axis=0)
+
+
+def lse_bounds_for_rows(x, rows, sel_of_row, scale: float) -> np.ndarray:
+    q = x.q.view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1, 128, 512)
+    return np.stack([lse_bound(q[r], candidate_records(x, r, sel_of_row(r)), scale) for r in rows])
+
+
+def check_attention(gpu_out: np.ndarray, gpu_lse: np.ndarray, ora_out: np.ndarray, ora_lse: np.ndarray, what: str,
+                    lse_tol: np.ndarray | None = None):
+    """gpu_out/ora_out [rows, H, D], lse_tol [rows, H] (max_j B_j); returns
+    (min cosine, max rel err, max lse err / bound)."""
     g = gpu_out.astype(np.float64)
     o = ora_out
     assert np.all(np.isfinite(g)), f"{what}: non-finite output"
@@ -121,8 +161,11 @@ def check_attention(gpu_out: np.ndarray, gpu_lse: np.ndarray, ora_out: np.ndarra
     lse_err = np.where(np.isneginf(ora_lse) & np.isneginf(gpu_lse), 0.0, lse_err)
     assert cos.min() >= ATT_COS_MIN, f"{what}: min per-head cosine {cos.min():.6f}"
     assert rel.max() <= ATT_MAXREL, f"{what}: max rel err {rel.max():.4g}"
-    assert lse_err.max() <= LSE_ATOL, f"{what}: lse err {lse_err.max():.3g}"
-    return float(cos.min()), float(rel.max()), float(lse_err.max())
+    bound = (np.zeros_like(lse_err) + LSE_ATOL) if lse_tol is None else \
+        lse_tol + 1e-5 * (1 + np.abs(np.where(np.isfinite(ora_lse), ora_lse, 0)))
+    ratio = lse_err / bound
+    assert ratio.max() <= 1.0, f"{what}: lse err {lse_err.max():.3g} ({ratio.max():.3g} x bound)"
+    return float(cos.min()), float(rel.max()), float(ratio.max())
 
 
 def oracle_cache(x) -> oracle.Cache:
