@@ -388,8 +388,12 @@ attention_tc_kernel(const AttParams P) {
                 z[c] = ((mask >> c) & 1ull) ? z[c] * P.scale_log2 : -INFINITY;
                 mx = fmaxf(mx, z[c]);
             }
-            if (mx > m + kLazy || (m == -INFINITY && mx > -INFINITY)) {
-                const float alpha = exp2f(m - mx);  // 0 when m = -inf
+            // Lazy rescale. The decision is per head (lane) but the TMEM accesses
+            // and waits below are warp-collective, so the whole warp enters
+            // when any lane needs it; other lanes use a factor of 1.
+            const bool need = mx > m + kLazy || (m == -INFINITY && mx > -INFINITY);
+            if (__any_sync(0xffffffffu, need)) {
+                const float alpha = need ? exp2f(m - mx) : 1.f;  // 0 when m = -inf
                 if (j > 0) {
                     // O holds PV of chunks < j: wait for the last one, then rescale in place
                     if (!wait(&s.o_done, (j - 1) & 1)) { fail(); ok = false; break; }
@@ -406,7 +410,7 @@ attention_tc_kernel(const AttParams P) {
                     ptx::tmem_st_wait();
                 }
                 l *= alpha;
-                m = mx;
+                if (need) m = mx;
             }
             uint32_t pk[32];
             float psum = 0.f;
