@@ -40,6 +40,8 @@ namespace {
 constexpr int kChunk = 64;                  // candidates per chunk
 constexpr int kHalf = 256;                  // latent dims per CTA
 constexpr int kSlot = 336;                  // staged bytes per candidate
+constexpr int kStages = 4;                  // staging ring depth (chunks)
+constexpr int kBatch = 4;                   // chunks whose indices the producer loads at once
 constexpr int kThreads = 320;               // 10 warps
 constexpr int kAtom = kChunk * 128;         // one 64-dim column block of X: 64 rows x 128 B
 constexpr int kXBytes = 4 * kAtom;          // 32 KB
@@ -56,9 +58,10 @@ constexpr uint32_t kTmemCols = 512;
 struct AttSmem {
     alignas(1024) uint8_t x[2][kXBytes];        // dequantised candidates, 128-byte swizzle
     alignas(1024) float4 recv[2][16 * kHeads];  // peer's partial scores: [16 float4][128 heads]
-    alignas(128) uint8_t stage[2][kChunk * kSlot];
-    uint64_t vmask[2], smask[2];
-    uint64_t stg_full[2], stg_empty[2], x_full[2], x_empty[2], s_full[2], p_full[2];
+    alignas(128) uint8_t stage[kStages][kChunk * kSlot];
+    uint64_t vmask[kStages], smask[2];
+    uint64_t stg_full[kStages], stg_empty[kStages];
+    uint64_t x_full[2], x_empty[2], s_full[2], p_full[2];
     uint64_t xchg_full[2], xchg_free[2];
     uint64_t o_done, q_ready, mma_done;
     uint32_t tmem_base;
@@ -149,15 +152,17 @@ attention_tc_kernel(const AttParams P) {
     const Unit u = make_unit(P);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kStages; ++i) {
             ptx::mbar_init(&s.stg_full[i], 32);
             ptx::mbar_init(&s.stg_empty[i], 4);
+        }
+        for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&s.x_full[i], 4);
             ptx::mbar_init(&s.x_empty[i], 1);
             ptx::mbar_init(&s.s_full[i], 1);
             ptx::mbar_init(&s.p_full[i], 4);
-            ptx::mbar_init(&s.xchg_full[i], 128);
-            ptx::mbar_init(&s.xchg_free[i], 128);
+            ptx::mbar_init(&s.xchg_full[i], 1);  // local expect_tx + the peer's st.async bytes
+            ptx::mbar_init(&s.xchg_free[i], 4);  // one release-arrive per peer softmax warp
         }
         ptx::mbar_init(&s.o_done, 1);
         ptx::mbar_init(&s.q_ready, 4);
@@ -185,48 +190,72 @@ attention_tc_kernel(const AttParams P) {
 
     if (warp == 0) {
         // ------------------------------------------------------------ gather producer
+        // Candidate indices are loaded one batch (4 chunks) ahead; lane L holds
+        // candidates L + 32 q (q = 0..7) of the batch, i.e. candidates L and
+        // L + 32 of each of its 4 chunks.
+        auto load_raw = [&](int g, int (&raw)[2 * kBatch]) {
+#pragma unroll
+            for (int q = 0; q < 2 * kBatch; ++q) {
+                const int i = u.cb + g * kBatch * kChunk + q * 32 + lane;
+                raw[q] = (!P.hca && i < u.ce && i < u.n_sel) ? __ldg(P.topk_idx + (size_t)u.r * P.k + i) : i;
+            }
+        };
+        const int n_batches = (u.n_chunks + kBatch - 1) / kBatch;
+        int cur[2 * kBatch], nxt[2 * kBatch];
+        if (n_batches > 0) load_raw(0, nxt);
         int j = 0;
         bool ok = true;
-        for (; j < u.n_chunks && ok; ++j) {
-            const int jb = j & 1;
-            if (!wait(&s.stg_empty[jb], ((j >> 1) & 1) ^ 1)) { fail(); ok = false; break; }
-            bool valid[2];
-            const uint8_t *rec[2];
-            uint32_t bytes = 0;
+        for (int g = 0; g < n_batches && ok; ++g) {
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int ci = 2 * lane + e;
-                const int i = u.cb + j * kChunk + ci;
-                rec[e] = i < u.ce ? candidate(P, u, i) : nullptr;
-                valid[e] = rec[e] != nullptr;
-                if (i < u.ce && !valid[e] && rank == 0) report_error(P.err, CSA_ERR_BAD_INDEX);
-                bytes += valid[e] ? (rank == 0 ? 272u : 336u) : 0u;
-            }
-            if (bytes) ptx::mbar_expect_tx(&s.stg_full[jb], bytes);
+            for (int q = 0; q < 2 * kBatch; ++q) cur[q] = nxt[q];
+            if (g + 1 < n_batches) load_raw(g + 1, nxt);
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                if (!valid[e]) continue;
-                uint8_t *dst = s.stage[jb] + (2 * lane + e) * kSlot;
-                if (rank == 0) {
-                    ptx::bulk_g2s(dst, rec[e], 256, &s.stg_full[jb]);
-                    ptx::bulk_g2s(dst + 256, rec[e] + kScaleOffset, 16, &s.stg_full[jb]);
-                } else {
-                    ptx::bulk_g2s(dst, rec[e] + 256, 336, &s.stg_full[jb]);
+            for (int cc = 0; cc < kBatch; ++cc) {
+                if (j >= u.n_chunks || !ok) break;
+                const int st = j % kStages;
+                if (!wait(&s.stg_empty[st], ((j / kStages) & 1) ^ 1)) { fail(); ok = false; break; }
+                bool valid[2];
+                const uint8_t *rec[2];
+                uint32_t bytes = 0;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int i = u.cb + j * kChunk + e * 32 + lane;
+                    rec[e] = nullptr;
+                    if (i < u.ce) {
+                        if (i < u.n_sel) {
+                            const int64_t ri = record_index(P.comp, u.b, cur[2 * cc + e]);
+                            if (ri >= 0) rec[e] = P.comp.base + ri * kRecBytes;
+                            else if (rank == 0) report_error(P.err, CSA_ERR_BAD_INDEX);
+                        } else {
+                            const int pos = u.j0 + (i - u.n_sel);
+                            rec[e] = P.ring + ((int64_t)u.b * P.R + pos % P.R) * kRecBytes;
+                        }
+                    }
+                    valid[e] = rec[e] != nullptr;
+                    bytes += valid[e] ? (rank == 0 ? 272u : 336u) : 0u;
                 }
+                if (bytes) ptx::mbar_expect_tx(&s.stg_full[st], bytes);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    if (!valid[e]) continue;
+                    uint8_t *dst = s.stage[st] + (e * 32 + lane) * kSlot;
+                    if (rank == 0) {
+                        ptx::bulk_g2s(dst, rec[e], 256, &s.stg_full[st]);
+                        ptx::bulk_g2s(dst + 256, rec[e] + kScaleOffset, 16, &s.stg_full[st]);
+                    } else {
+                        ptx::bulk_g2s(dst, rec[e] + 256, 336, &s.stg_full[st]);
+                    }
+                }
+                const uint32_t m0 = __ballot_sync(0xffffffffu, valid[0]);
+                const uint32_t m1 = __ballot_sync(0xffffffffu, valid[1]);
+                if (lane == 0) s.vmask[st] = (uint64_t)m0 | ((uint64_t)m1 << 32);
+                __syncwarp();
+                ptx::mbar_arrive(&s.stg_full[st]);
+                ++j;
             }
-            const uint32_t m0 = __ballot_sync(0xffffffffu, valid[0]);
-            const uint32_t m1 = __ballot_sync(0xffffffffu, valid[1]);
-            if (lane == 0) {
-                uint64_t mask = 0;
-                for (int L = 0; L < 32; ++L)
-                    mask |= (uint64_t)((m0 >> L) & 1u) << (2 * L) | (uint64_t)((m1 >> L) & 1u) << (2 * L + 1);
-                s.vmask[jb] = mask;
-            }
-            __syncwarp();
-            ptx::mbar_arrive(&s.stg_full[jb]);
         }
         // drain: every issued copy has landed before the CTA may exit
-        for (int q = (j > 2 ? j - 2 : 0); q < j; ++q) wait(&s.stg_full[q & 1], (q >> 1) & 1);
+        for (int q = (j > kStages ? j - kStages : 0); q < j; ++q) wait(&s.stg_full[q % kStages], (q / kStages) & 1);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         constexpr uint32_t kIdescQK = ptx::idesc_f32acc(1, 1, 128, kChunk);
@@ -278,11 +307,12 @@ attention_tc_kernel(const AttParams P) {
         bool ok = true;
         for (int j = 0; j < u.n_chunks && ok; ++j) {
             const int jb = j & 1;
-            if (!wait(&s.stg_full[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
+            const int st = j % kStages;
+            if (!wait(&s.stg_full[st], (j / kStages) & 1)) { fail(); ok = false; break; }
             if (!wait(&s.x_empty[jb], ((j >> 1) & 1) ^ 1)) { fail(); ok = false; break; }
-            const uint64_t mask = s.vmask[jb];
+            const uint64_t mask = s.vmask[st];
             const bool valid = (mask >> ci) & 1ull;
-            const uint8_t *slot = s.stage[jb] + ci * kSlot;
+            const uint8_t *slot = s.stage[st] + ci * kSlot;
             uint8_t *xrow = s.x[jb] + ci * 128;
 #pragma unroll
             for (int aa = 0; aa < 2; ++aa) {
@@ -309,7 +339,7 @@ attention_tc_kernel(const AttParams P) {
             if (ct == 0) s.smask[jb] = mask;
             __syncwarp();
             if (lane == 0) {
-                ptx::mbar_arrive(&s.stg_empty[jb]);
+                ptx::mbar_arrive(&s.stg_empty[st]);
                 ptx::mbar_arrive(&s.x_full[jb]);
             }
         }
@@ -356,18 +386,21 @@ attention_tc_kernel(const AttParams P) {
             ptx::tmem_ld32(lane_base + kColS + jb * kChunk, sa);
             ptx::tmem_ld32(lane_base + kColS + jb * kChunk + 32, sb);
             ptx::tmem_ld_wait();
-            // exchange partial scores with the peer CTA
+            // exchange partial scores with the peer CTA: st.async into its
+            // receive buffer, completing bytes on its xchg_full barrier
+            if (threadIdx.x == 192) ptx::mbar_arrive_expect_tx(&s.xchg_full[jb], 16 * kHeads * 16);
             if (j >= 2 && !wait_cluster(&s.xchg_free[jb], ((j - 2) >> 1) & 1)) { fail(); ok = false; break; }
 #pragma unroll
             for (int cq = 0; cq < 8; ++cq) {
-                ptx::st_cluster_v4(recv_peer[jb] + (uint32_t)((cq * kHeads + h) * 16),
-                                   make_float4(__uint_as_float(sa[4 * cq]), __uint_as_float(sa[4 * cq + 1]),
-                                               __uint_as_float(sa[4 * cq + 2]), __uint_as_float(sa[4 * cq + 3])));
-                ptx::st_cluster_v4(recv_peer[jb] + (uint32_t)(((8 + cq) * kHeads + h) * 16),
-                                   make_float4(__uint_as_float(sb[4 * cq]), __uint_as_float(sb[4 * cq + 1]),
-                                               __uint_as_float(sb[4 * cq + 2]), __uint_as_float(sb[4 * cq + 3])));
+                ptx::st_async_v4(recv_peer[jb] + (uint32_t)((cq * kHeads + h) * 16),
+                                 make_float4(__uint_as_float(sa[4 * cq]), __uint_as_float(sa[4 * cq + 1]),
+                                             __uint_as_float(sa[4 * cq + 2]), __uint_as_float(sa[4 * cq + 3])),
+                                 full_peer[jb]);
+                ptx::st_async_v4(recv_peer[jb] + (uint32_t)(((8 + cq) * kHeads + h) * 16),
+                                 make_float4(__uint_as_float(sb[4 * cq]), __uint_as_float(sb[4 * cq + 1]),
+                                             __uint_as_float(sb[4 * cq + 2]), __uint_as_float(sb[4 * cq + 3])),
+                                 full_peer[jb]);
             }
-            ptx::mbar_arrive_remote(full_peer[jb]);
             if (!wait_cluster(&s.xchg_full[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
             float z[kChunk];
 #pragma unroll
@@ -379,7 +412,8 @@ attention_tc_kernel(const AttParams P) {
                 z[4 * cq + 2] = __uint_as_float(own[2]) + pv.z;
                 z[4 * cq + 3] = __uint_as_float(own[3]) + pv.w;
             }
-            ptx::mbar_arrive_remote(free_peer[jb]);
+            __syncwarp();  // every lane has consumed its received scores
+            if (lane == 0) ptx::mbar_arrive_remote(free_peer[jb]);
             if (!wait(&s.x_full[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
             const uint64_t mask = s.smask[jb];
             float mx = -INFINITY;

@@ -301,5 +301,15 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
     }
 }
 
+
+// Asynchronous store of 16 bytes into another CTA's shared memory; completes
+// 16 transaction bytes on the mbarrier at `remote_bar` (same CTA as `addr`).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     addr),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+                 : "memory");
+}
+
 }  // namespace ptx
 }  // namespace csa
