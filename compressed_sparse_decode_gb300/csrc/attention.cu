@@ -111,17 +111,6 @@ __device__ __forceinline__ Unit make_unit(const AttParams &P) {
     return u;
 }
 
-// Record of candidate i of the unit's list, or nullptr (outside the cache).
-__device__ __forceinline__ const uint8_t *candidate(const AttParams &P, const Unit &u, int i) {
-    if (i < u.n_sel) {
-        const int c = P.hca ? i : __ldg(P.topk_idx + (size_t)u.r * P.k + i);
-        const int64_t rec = record_index(P.comp, u.b, c);
-        return rec < 0 ? nullptr : P.comp.base + rec * kRecBytes;
-    }
-    const int pos = u.j0 + (i - u.n_sel);
-    return P.ring + ((int64_t)u.b * P.R + pos % P.R) * kRecBytes;
-}
-
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -141,6 +130,19 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w0, uint32_t w1, float s) {
     return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
+// 16 E4M3 codes times a multiplier -> 16 BF16 values (two uint4).
+__device__ __forceinline__ void dequant16(uint4 c, float s, uint4 &lo, uint4 &hi) {
+    lo = dequant8(c.x, c.y, s);
+    hi = dequant8(c.z, c.w, s);
+}
+
+// One 64-dim block of a candidate row of X: dims [64 a, 64 a + 64) of this
+// CTA's half; chunk cc of the 128-byte row lands at position cc ^ (row & 7).
+__device__ __forceinline__ void store_atom_row(uint8_t *xa, int row, const uint4 (&v)[8]) {
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4 *>(xa + ((cc ^ (row & 7)) << 4)) = v[cc];
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 attention_tc_kernel(const AttParams P) {
     extern __shared__ uint8_t smem_raw[];
@@ -153,7 +155,7 @@ attention_tc_kernel(const AttParams P) {
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            ptx::mbar_init(&s.stg_full[i], 32);
+            ptx::mbar_init(&s.stg_full[i], 64);  // 32 copy-completion arrivals + 32 lane arrivals
             ptx::mbar_init(&s.stg_empty[i], 4);
         }
         for (int i = 0; i < 2; ++i) {
@@ -216,7 +218,6 @@ attention_tc_kernel(const AttParams P) {
                 if (!wait(&s.stg_empty[st], ((j / kStages) & 1) ^ 1)) { fail(); ok = false; break; }
                 bool valid[2];
                 const uint8_t *rec[2];
-                uint32_t bytes = 0;
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int i = u.cb + j * kChunk + e * 32 + lane;
@@ -232,20 +233,23 @@ attention_tc_kernel(const AttParams P) {
                         }
                     }
                     valid[e] = rec[e] != nullptr;
-                    bytes += valid[e] ? (rank == 0 ? 272u : 336u) : 0u;
                 }
-                if (bytes) ptx::mbar_expect_tx(&s.stg_full[st], bytes);
+                // each lane copies its two candidates' bytes in 16-byte pieces:
+                // rank 0 bytes [0,256) + [576,592), rank 1 bytes [256,592)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     if (!valid[e]) continue;
                     uint8_t *dst = s.stage[st] + (e * 32 + lane) * kSlot;
                     if (rank == 0) {
-                        ptx::bulk_g2s(dst, rec[e], 256, &s.stg_full[st]);
-                        ptx::bulk_g2s(dst + 256, rec[e] + kScaleOffset, 16, &s.stg_full[st]);
+#pragma unroll
+                        for (int pc = 0; pc < 16; ++pc) ptx::cp_async_16(dst + pc * 16, rec[e] + pc * 16);
+                        ptx::cp_async_16(dst + 256, rec[e] + kScaleOffset);
                     } else {
-                        ptx::bulk_g2s(dst, rec[e] + 256, 336, &s.stg_full[st]);
+#pragma unroll
+                        for (int pc = 0; pc < 21; ++pc) ptx::cp_async_16(dst + pc * 16, rec[e] + 256 + pc * 16);
                     }
                 }
+                ptx::cp_async_arrive_noinc(&s.stg_full[st]);
                 const uint32_t m0 = __ballot_sync(0xffffffffu, valid[0]);
                 const uint32_t m1 = __ballot_sync(0xffffffffu, valid[1]);
                 if (lane == 0) s.vmask[st] = (uint64_t)m0 | ((uint64_t)m1 << 32);
@@ -314,27 +318,37 @@ attention_tc_kernel(const AttParams P) {
             const bool valid = (mask >> ci) & 1ull;
             const uint8_t *slot = s.stage[st] + ci * kSlot;
             uint8_t *xrow = s.x[jb] + ci * 128;
+            // this thread's two 64-dim blocks of the row: local dims [128 half, 128 half + 128)
+            // rank 0: latent dims 128 half + ..., one multiplier (block `half`)
+            // rank 1: half 0 -> latent 256..383 (block 2); half 1 -> latent 384..447
+            //         (block 3) then the 64 rope dims (BF16, copied)
+            uint4 v[2][8];
+            if (valid) {
+                const uint4 *codes = reinterpret_cast<const uint4 *>(slot + 128 * half);
+                if (rank == 0 || half == 0) {
+                    const float sc = *reinterpret_cast<const float *>(slot + (rank == 0 ? 256 + 4 * half : 320 + 8));
+                    uint4 cv[8];
 #pragma unroll
-            for (int aa = 0; aa < 2; ++aa) {
-                const int atom = 2 * half + aa;  // local dims [64 atom, 64 atom + 64)
-                uint8_t *xa = xrow + atom * kAtom;
+                    for (int q = 0; q < 8; ++q) cv[q] = codes[q];
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const int d = atom * 64 + cc * 8;  // first local dim of this 16-byte chunk
-                    uint4 v = make_uint4(0, 0, 0, 0);
-                    if (valid) {
-                        if (rank == 1 && d >= 192) {
-                            v = *reinterpret_cast<const uint4 *>(slot + 192 + (d - 192) * 2);  // rope, BF16
-                        } else {
-                            const uint2 codes = *reinterpret_cast<const uint2 *>(slot + d);
-                            const int blk = (rank == 0 ? d : 256 + d) >> 7;
-                            const float sc = *reinterpret_cast<const float *>(slot + (rank == 0 ? 256 : 320) + 4 * blk);
-                            v = dequant8(codes.x, codes.y, sc);
-                        }
-                    }
-                    *reinterpret_cast<uint4 *>(xa + ((cc ^ (ci & 7)) << 4)) = v;
+                    for (int q = 0; q < 8; ++q) dequant16(cv[q], sc, v[q >> 2][(q & 3) * 2], v[q >> 2][(q & 3) * 2 + 1]);
+                } else {
+                    const float sc = *reinterpret_cast<const float *>(slot + 320 + 12);
+                    uint4 cv[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) cv[q] = codes[q];
+                    const uint4 *rope = reinterpret_cast<const uint4 *>(slot + 192);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) v[1][q] = rope[q];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) dequant16(cv[q], sc, v[0][2 * q], v[0][2 * q + 1]);
                 }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) v[0][q] = v[1][q] = make_uint4(0, 0, 0, 0);
             }
+            store_atom_row(xrow + (2 * half) * kAtom, ci, v[0]);
+            store_atom_row(xrow + (2 * half + 1) * kAtom, ci, v[1]);
             ptx::fence_proxy_async_smem();  // generic-proxy stores -> MMA (async proxy) reads
             if (ct == 0) s.smask[jb] = mask;
             __syncwarp();
@@ -378,30 +392,43 @@ attention_tc_kernel(const AttParams P) {
         const uint32_t free_peer[2] = {ptx::mapa(ptx::smem_u32(&s.xchg_free[0]), peer),
                                        ptx::mapa(ptx::smem_u32(&s.xchg_free[1]), peer)};
         float m = -INFINITY, l = 0.f;  // running max and sum, log2 domain, sink not included
+        // Sends this CTA's partial scores of chunk jj to the peer (st.async,
+        // completing bytes on the peer's xchg_full barrier) and arms the local
+        // receive barrier of chunk jj. Chunk j+1 is sent before chunk j is
+        // combined, so the exchange round trip overlaps the softmax of chunk j.
+        auto send = [&](int jj) -> bool {
+            const int b2 = jj & 1;
+            if (!wait(&s.s_full[b2], (jj >> 1) & 1)) return false;
+            ptx::tc_fence_after();
+            uint32_t sa[32], sb[32];
+            ptx::tmem_ld32(lane_base + kColS + b2 * kChunk, sa);
+            ptx::tmem_ld32(lane_base + kColS + b2 * kChunk + 32, sb);
+            ptx::tmem_ld_wait();
+            if (threadIdx.x == 192) ptx::mbar_arrive_expect_tx(&s.xchg_full[b2], 16 * kHeads * 16);
+            if (jj >= 2 && !wait_cluster(&s.xchg_free[b2], ((jj - 2) >> 1) & 1)) return false;
+#pragma unroll
+            for (int cq = 0; cq < 8; ++cq) {
+                ptx::st_async_v4(recv_peer[b2] + (uint32_t)((cq * kHeads + h) * 16),
+                                 make_float4(__uint_as_float(sa[4 * cq]), __uint_as_float(sa[4 * cq + 1]),
+                                             __uint_as_float(sa[4 * cq + 2]), __uint_as_float(sa[4 * cq + 3])),
+                                 full_peer[b2]);
+                ptx::st_async_v4(recv_peer[b2] + (uint32_t)(((8 + cq) * kHeads + h) * 16),
+                                 make_float4(__uint_as_float(sb[4 * cq]), __uint_as_float(sb[4 * cq + 1]),
+                                             __uint_as_float(sb[4 * cq + 2]), __uint_as_float(sb[4 * cq + 3])),
+                                 full_peer[b2]);
+            }
+            return true;
+        };
+        if (u.n_chunks > 0 && !send(0)) { fail(); ok = false; }
         for (int j = 0; j < u.n_chunks && ok; ++j) {
             const int jb = j & 1;
-            if (!wait(&s.s_full[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
-            ptx::tc_fence_after();
+            if (j + 1 < u.n_chunks && !send(j + 1)) { fail(); ok = false; break; }
+            if (!wait_cluster(&s.xchg_full[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
+            // own partial of chunk j (still in TMEM: P(j) has not been written yet)
             uint32_t sa[32], sb[32];
             ptx::tmem_ld32(lane_base + kColS + jb * kChunk, sa);
             ptx::tmem_ld32(lane_base + kColS + jb * kChunk + 32, sb);
             ptx::tmem_ld_wait();
-            // exchange partial scores with the peer CTA: st.async into its
-            // receive buffer, completing bytes on its xchg_full barrier
-            if (threadIdx.x == 192) ptx::mbar_arrive_expect_tx(&s.xchg_full[jb], 16 * kHeads * 16);
-            if (j >= 2 && !wait_cluster(&s.xchg_free[jb], ((j - 2) >> 1) & 1)) { fail(); ok = false; break; }
-#pragma unroll
-            for (int cq = 0; cq < 8; ++cq) {
-                ptx::st_async_v4(recv_peer[jb] + (uint32_t)((cq * kHeads + h) * 16),
-                                 make_float4(__uint_as_float(sa[4 * cq]), __uint_as_float(sa[4 * cq + 1]),
-                                             __uint_as_float(sa[4 * cq + 2]), __uint_as_float(sa[4 * cq + 3])),
-                                 full_peer[jb]);
-                ptx::st_async_v4(recv_peer[jb] + (uint32_t)(((8 + cq) * kHeads + h) * 16),
-                                 make_float4(__uint_as_float(sb[4 * cq]), __uint_as_float(sb[4 * cq + 1]),
-                                             __uint_as_float(sb[4 * cq + 2]), __uint_as_float(sb[4 * cq + 3])),
-                                 full_peer[jb]);
-            }
-            if (!wait_cluster(&s.xchg_full[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
             float z[kChunk];
 #pragma unroll
             for (int cq = 0; cq < 16; ++cq) {
@@ -427,7 +454,7 @@ attention_tc_kernel(const AttParams P) {
             // when any lane needs it; other lanes use a factor of 1.
             const bool need = mx > m + kLazy || (m == -INFINITY && mx > -INFINITY);
             if (__any_sync(0xffffffffu, need)) {
-                const float alpha = need ? exp2f(m - mx) : 1.f;  // 0 when m = -inf
+                const float alpha = need ? ptx::ex2_approx(m - mx) : 1.f;  // 0 when m = -inf
                 if (j > 0) {
                     // O holds PV of chunks < j: wait for the last one, then rescale in place
                     if (!wait(&s.o_done, (j - 1) & 1)) { fail(); ok = false; break; }
@@ -451,7 +478,7 @@ attention_tc_kernel(const AttParams P) {
             const float mref = (m == -INFINITY) ? 0.f : m;  // every z is -inf while m is
 #pragma unroll
             for (int c2 = 0; c2 < kChunk / 2; ++c2) {
-                const float p0 = exp2f(z[2 * c2] - mref), p1 = exp2f(z[2 * c2 + 1] - mref);
+                const float p0 = ptx::ex2_approx(z[2 * c2] - mref), p1 = ptx::ex2_approx(z[2 * c2 + 1] - mref);
                 psum += p0 + p1;
                 pk[c2] = bf16x2_bits(p0, p1);
             }
