@@ -40,7 +40,8 @@ namespace {
 constexpr int kChunk = 64;                  // candidates per chunk
 constexpr int kHalf = 256;                  // latent dims per CTA
 constexpr int kSlot = 336;                  // staged bytes per candidate
-constexpr int kStages = 4;                  // staging ring depth (chunks)
+constexpr int kStages = 2;                  // staging ring depth (chunks)
+constexpr int kXBuf = 3;                    // dequantised chunk buffers
 constexpr int kBatch = 4;                   // chunks whose indices the producer loads at once
 constexpr int kThreads = 320;               // 10 warps
 constexpr int kAtom = kChunk * 128;         // one 64-dim column block of X: 64 rows x 128 B
@@ -52,16 +53,20 @@ constexpr float kLazy = 8.f;                // rescale only when the max grows b
 
 constexpr uint32_t kColQ = 0;    // 128 columns: Q half, BF16 pairs
 constexpr uint32_t kColO = 128;  // 256 columns: O half, fp32
-constexpr uint32_t kColS = 384;  // 2 x 64 columns: scores, then P (BF16 pairs) in the first 32
+constexpr uint32_t kColS = 384;  // 2 x 64 columns: partial scores
 constexpr uint32_t kTmemCols = 512;
 
+// recv[b] first receives the peer's partial scores of a chunk ([16 float4]
+// [128 heads], fp32), then holds that chunk's P (128 heads x 64 candidates,
+// BF16, K-major rows of 128 B in the 128-byte swizzle) as the A operand of PV.
 struct AttSmem {
-    alignas(1024) uint8_t x[2][kXBytes];        // dequantised candidates, 128-byte swizzle
-    alignas(1024) float4 recv[2][16 * kHeads];  // peer's partial scores: [16 float4][128 heads]
+    alignas(1024) uint8_t x[kXBuf][kXBytes];    // dequantised candidates, 128-byte swizzle
+    alignas(1024) float4 recv[2][16 * kHeads];
     alignas(128) uint8_t stage[kStages][kChunk * kSlot];
-    uint64_t vmask[kStages], smask[2];
+    uint64_t vmask[kStages], smask[kXBuf];
     uint64_t stg_full[kStages], stg_empty[kStages];
-    uint64_t x_full[2], x_empty[2], s_full[2], p_full[2];
+    uint64_t x_full[kXBuf], x_empty[kXBuf];
+    uint64_t s_full[2], s_free[2], p_full[2], rd_done[2];
     uint64_t xchg_full[2], xchg_free[2];
     uint64_t o_done, q_ready, mma_done;
     uint32_t tmem_base;
@@ -136,13 +141,23 @@ __device__ __forceinline__ void dequant16(uint4 c, float s, uint4 &lo, uint4 &hi
     hi = dequant8(c.z, c.w, s);
 }
 
-// One 64-dim block of a candidate row of X: dims [64 a, 64 a + 64) of this
-// CTA's half; chunk cc of the 128-byte row lands at position cc ^ (row & 7).
+// One 64-dim block of a row in the 128-byte swizzle: 16-byte chunk cc of the
+// 128-byte row lands at position cc ^ (row & 7).
 __device__ __forceinline__ void store_atom_row(uint8_t *xa, int row, const uint4 (&v)[8]) {
 #pragma unroll
     for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4 *>(xa + ((cc ^ (row & 7)) << 4)) = v[cc];
 }
 
+// Pipeline per chunk j (64 candidates), per CTA of the pair:
+//   producer:  gather raw bytes of chunk j            -> stage[j % 2]
+//   dequant:   stage -> X[j % 3] (BF16)               (after PV(j-3) freed it)
+//   MMA:       QK(j) -> S[j & 1] (after the softmax released S(j-2));
+//              PV(j) = P(j) X(j) -> O (after P(j) is ready); QK(j+2) is
+//              issued before PV(j), so scores run two chunks ahead
+//   softmax:   sends S(j+1) to the peer, combines S(j) with the peer's
+//              partial, releases S[j & 1], writes P(j) into recv[j & 1]
+//   PV(j) completion frees X[j % 3] and, by a multicast commit, tells the
+//   peer that it may write chunk j+2's partial into this CTA's recv[j & 1].
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 attention_tc_kernel(const AttParams P) {
     extern __shared__ uint8_t smem_raw[];
@@ -158,13 +173,17 @@ attention_tc_kernel(const AttParams P) {
             ptx::mbar_init(&s.stg_full[i], 64);  // 32 copy-completion arrivals + 32 lane arrivals
             ptx::mbar_init(&s.stg_empty[i], 4);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kXBuf; ++i) {
             ptx::mbar_init(&s.x_full[i], 4);
             ptx::mbar_init(&s.x_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&s.s_full[i], 1);
+            ptx::mbar_init(&s.s_free[i], 4);
             ptx::mbar_init(&s.p_full[i], 4);
+            ptx::mbar_init(&s.rd_done[i], 4);  // every softmax warp has read recv[i]
             ptx::mbar_init(&s.xchg_full[i], 1);  // local expect_tx + the peer's st.async bytes
-            ptx::mbar_init(&s.xchg_free[i], 4);  // one release-arrive per peer softmax warp
+            ptx::mbar_init(&s.xchg_free[i], 1);  // the peer's multicast commit after its PV
         }
         ptx::mbar_init(&s.o_done, 1);
         ptx::mbar_init(&s.q_ready, 4);
@@ -266,40 +285,48 @@ attention_tc_kernel(const AttParams P) {
         constexpr uint32_t kIdescPV = ptx::idesc_f32acc(1, 1, 128, kHalf, 1);
         bool ok = u.n_chunks == 0 || wait(&s.q_ready, 0);
         if (!ok) fail();
-        auto issue_pv = [&](int jp) -> bool {
-            const int pb = jp & 1;
-            if (!wait(&s.p_full[pb], (jp >> 1) & 1)) return false;
+        auto issue_qk = [&](int jq) -> bool {
+            const int xb = jq % kXBuf, sb = jq & 1;
+            if (!wait(&s.x_full[xb], (jq / kXBuf) & 1)) return false;
+            if (jq >= 2 && !wait(&s.s_free[sb], ((jq - 2) >> 1) & 1)) return false;
             ptx::tc_fence_after();
             if (lane == 0) {
-                const uint32_t xb = ptx::smem_u32(s.x[pb]);
+                const uint32_t xa = ptx::smem_u32(s.x[xb]);
 #pragma unroll
-                for (int kk = 0; kk < kChunk / 16; ++kk)
-                    ptx::mma_f16_ts(tmem + kColO, tmem + kColS + pb * kChunk + kk * 8,
-                                    ptx::desc_mnmajor_sw128(xb + kk * 2048, kAtom, 1024), kIdescPV,
-                                    (jp > 0 || kk > 0) ? 1u : 0u);
-                ptx::mma_commit(&s.x_empty[pb]);
-                ptx::mma_commit(&s.o_done);
+                for (int kk = 0; kk < kHalf / 16; ++kk)
+                    ptx::mma_f16_ts(tmem + kColS + sb * kChunk, tmem + kColQ + kk * 8,
+                                    ptx::desc_kmajor_sw128(xa + (kk >> 2) * kAtom + (kk & 3) * 32), kIdescQK,
+                                    kk > 0 ? 1u : 0u);
+                ptx::mma_commit(&s.s_full[sb]);
             }
             __syncwarp();
             return true;
         };
-        for (int j = 0; j < u.n_chunks && ok; ++j) {
-            const int jb = j & 1;
-            if (!wait(&s.x_full[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
+        auto issue_pv = [&](int jp) -> bool {
+            const int xb = jp % kXBuf, pb = jp & 1;
+            if (!wait(&s.p_full[pb], (jp >> 1) & 1)) return false;
             ptx::tc_fence_after();
             if (lane == 0) {
-                const uint32_t xb = ptx::smem_u32(s.x[jb]);
+                const uint32_t xa = ptx::smem_u32(s.x[xb]);
+                const uint32_t pa = ptx::smem_u32(s.recv[pb]);
 #pragma unroll
-                for (int kk = 0; kk < kHalf / 16; ++kk)
-                    ptx::mma_f16_ts(tmem + kColS + jb * kChunk, tmem + kColQ + kk * 8,
-                                    ptx::desc_kmajor_sw128(xb + (kk >> 2) * kAtom + (kk & 3) * 32), kIdescQK,
-                                    kk > 0 ? 1u : 0u);
-                ptx::mma_commit(&s.s_full[jb]);
+                for (int kk = 0; kk < kChunk / 16; ++kk)
+                    ptx::mma_f16(tmem + kColO, ptx::desc_kmajor_sw128(pa + kk * 32),
+                                 ptx::desc_mnmajor_sw128(xa + kk * 2048, kAtom, 1024), kIdescPV,
+                                 (jp > 0 || kk > 0) ? 1u : 0u);
+                ptx::mma_commit(&s.x_empty[xb]);
+                ptx::mma_commit(&s.o_done);
+                ptx::mma_commit_multicast(&s.xchg_free[pb], static_cast<uint16_t>(1u << peer));
             }
             __syncwarp();
-            if (j > 0 && !issue_pv(j - 1)) { fail(); ok = false; break; }
+            return true;
+        };
+        if (ok && u.n_chunks > 0 && !issue_qk(0)) { fail(); ok = false; }
+        if (ok && u.n_chunks > 1 && !issue_qk(1)) { fail(); ok = false; }
+        for (int j = 0; j < u.n_chunks && ok; ++j) {
+            if (j + 2 < u.n_chunks && !issue_qk(j + 2)) { fail(); ok = false; break; }
+            if (!issue_pv(j)) { fail(); ok = false; break; }
         }
-        if (ok && u.n_chunks > 0 && !issue_pv(u.n_chunks - 1)) fail();
         if (lane == 0) ptx::mma_commit(&s.mma_done);
         __syncwarp();
         wait(&s.mma_done, 0);
@@ -310,14 +337,13 @@ attention_tc_kernel(const AttParams P) {
         const int half = ct & 1;          // local dims [128 half, 128 half + 128)
         bool ok = true;
         for (int j = 0; j < u.n_chunks && ok; ++j) {
-            const int jb = j & 1;
-            const int st = j % kStages;
+            const int st = j % kStages, xb = j % kXBuf;
             if (!wait(&s.stg_full[st], (j / kStages) & 1)) { fail(); ok = false; break; }
-            if (!wait(&s.x_empty[jb], ((j >> 1) & 1) ^ 1)) { fail(); ok = false; break; }
+            if (!wait(&s.x_empty[xb], ((j / kXBuf) & 1) ^ 1)) { fail(); ok = false; break; }
             const uint64_t mask = s.vmask[st];
             const bool valid = (mask >> ci) & 1ull;
             const uint8_t *slot = s.stage[st] + ci * kSlot;
-            uint8_t *xrow = s.x[jb] + ci * 128;
+            uint8_t *xrow = s.x[xb] + ci * 128;
             // this thread's two 64-dim blocks of the row: local dims [128 half, 128 half + 128)
             // rank 0: latent dims 128 half + ..., one multiplier (block `half`)
             // rank 1: half 0 -> latent 256..383 (block 2); half 1 -> latent 384..447
@@ -350,11 +376,11 @@ attention_tc_kernel(const AttParams P) {
             store_atom_row(xrow + (2 * half) * kAtom, ci, v[0]);
             store_atom_row(xrow + (2 * half + 1) * kAtom, ci, v[1]);
             ptx::fence_proxy_async_smem();  // generic-proxy stores -> MMA (async proxy) reads
-            if (ct == 0) s.smask[jb] = mask;
+            if (ct == 0) s.smask[xb] = mask;
             __syncwarp();
             if (lane == 0) {
                 ptx::mbar_arrive(&s.stg_empty[st]);
-                ptx::mbar_arrive(&s.x_full[jb]);
+                ptx::mbar_arrive(&s.x_full[xb]);
             }
         }
     } else {
@@ -389,13 +415,11 @@ attention_tc_kernel(const AttParams P) {
                                        ptx::mapa(ptx::smem_u32(s.recv[1]), peer)};
         const uint32_t full_peer[2] = {ptx::mapa(ptx::smem_u32(&s.xchg_full[0]), peer),
                                        ptx::mapa(ptx::smem_u32(&s.xchg_full[1]), peer)};
-        const uint32_t free_peer[2] = {ptx::mapa(ptx::smem_u32(&s.xchg_free[0]), peer),
-                                       ptx::mapa(ptx::smem_u32(&s.xchg_free[1]), peer)};
         float m = -INFINITY, l = 0.f;  // running max and sum, log2 domain, sink not included
-        // Sends this CTA's partial scores of chunk jj to the peer (st.async,
-        // completing bytes on the peer's xchg_full barrier) and arms the local
-        // receive barrier of chunk jj. Chunk j+1 is sent before chunk j is
-        // combined, so the exchange round trip overlaps the softmax of chunk j.
+        // Sends this CTA's partial scores of chunk jj into the peer's recv
+        // (st.async, completing bytes on the peer's xchg_full barrier) once the
+        // peer's PV(jj-2) has released that buffer, and arms the local receive
+        // barrier of chunk jj.
         auto send = [&](int jj) -> bool {
             const int b2 = jj & 1;
             if (!wait(&s.s_full[b2], (jj >> 1) & 1)) return false;
@@ -421,14 +445,17 @@ attention_tc_kernel(const AttParams P) {
         };
         if (u.n_chunks > 0 && !send(0)) { fail(); ok = false; }
         for (int j = 0; j < u.n_chunks && ok; ++j) {
-            const int jb = j & 1;
+            const int jb = j & 1, xb = j % kXBuf;
             if (j + 1 < u.n_chunks && !send(j + 1)) { fail(); ok = false; break; }
             if (!wait_cluster(&s.xchg_full[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
-            // own partial of chunk j (still in TMEM: P(j) has not been written yet)
+            // own partial of chunk j from TMEM, then release the score buffer
             uint32_t sa[32], sb[32];
             ptx::tmem_ld32(lane_base + kColS + jb * kChunk, sa);
             ptx::tmem_ld32(lane_base + kColS + jb * kChunk + 32, sb);
             ptx::tmem_ld_wait();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&s.s_free[jb]);
             float z[kChunk];
 #pragma unroll
             for (int cq = 0; cq < 16; ++cq) {
@@ -439,16 +466,19 @@ attention_tc_kernel(const AttParams P) {
                 z[4 * cq + 2] = __uint_as_float(own[2]) + pv.z;
                 z[4 * cq + 3] = __uint_as_float(own[3]) + pv.w;
             }
-            __syncwarp();  // every lane has consumed its received scores
-            if (lane == 0) ptx::mbar_arrive_remote(free_peer[jb]);
-            if (!wait(&s.x_full[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
-            const uint64_t mask = s.smask[jb];
-            float mx = -INFINITY;
+            // every softmax thread has read recv[jb] before P overwrites it
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&s.rd_done[jb]);
+            if (!wait(&s.rd_done[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
+            if (!wait(&s.x_full[xb], (j / kXBuf) & 1)) { fail(); ok = false; break; }
+            const uint64_t mask = s.smask[xb];
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int c = 0; c < kChunk; ++c) {
                 z[c] = ((mask >> c) & 1ull) ? z[c] * P.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, z[c]);
+                mx4[c & 3] = fmaxf(mx4[c & 3], z[c]);
             }
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
             // Lazy rescale. The decision is per head (lane) but the TMEM accesses
             // and waits below are warp-collective, so the whole warp enters
             // when any lane needs it; other lanes use a factor of 1.
@@ -469,23 +499,29 @@ attention_tc_kernel(const AttParams P) {
                         ptx::tmem_st32(lane_base + kColO + piece * 32, o);
                     }
                     ptx::tmem_st_wait();
+                    ptx::tc_fence_before();
                 }
                 l *= alpha;
                 if (need) m = mx;
             }
-            uint32_t pk[32];
-            float psum = 0.f;
+            // P(j) = 2^(z - m) as BF16 rows in recv[jb] (K-major, 128-byte swizzle)
             const float mref = (m == -INFINITY) ? 0.f : m;  // every z is -inf while m is
+            float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+            uint8_t *prow = reinterpret_cast<uint8_t *>(s.recv[jb]) + h * 128;
 #pragma unroll
-            for (int c2 = 0; c2 < kChunk / 2; ++c2) {
-                const float p0 = ptx::ex2_approx(z[2 * c2] - mref), p1 = ptx::ex2_approx(z[2 * c2 + 1] - mref);
-                psum += p0 + p1;
-                pk[c2] = bf16x2_bits(p0, p1);
+            for (int c8 = 0; c8 < 8; ++c8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float p0 = ptx::ex2_approx(z[8 * c8 + 2 * i] - mref);
+                    const float p1 = ptx::ex2_approx(z[8 * c8 + 2 * i + 1] - mref);
+                    ps4[i] += p0 + p1;
+                    w[i] = bf16x2_bits(p0, p1);
+                }
+                *reinterpret_cast<uint4 *>(prow + ((c8 ^ (h & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            l += psum;
-            ptx::tmem_st32(lane_base + kColS + jb * kChunk, pk);
-            ptx::tmem_st_wait();
-            ptx::tc_fence_before();
+            l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+            ptx::fence_proxy_async_smem();  // P stores -> PV (async proxy) reads
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&s.p_full[jb]);
         }

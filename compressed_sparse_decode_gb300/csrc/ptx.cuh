@@ -332,5 +332,21 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+
+// Arrive (once) on the mbarrier at the same shared-memory offset in every CTA
+// of `cta_mask` when every MMA issued so far by this thread is done.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// Named barrier over `count` threads (id > 0; id 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 }  // namespace ptx
 }  // namespace csa
