@@ -56,19 +56,20 @@ constexpr uint32_t kColO = 128;  // 256 columns: O half, fp32
 constexpr uint32_t kColS = 384;  // 2 x 64 columns: partial scores
 constexpr uint32_t kTmemCols = 512;
 
-// recv[b] first receives the peer's partial scores of a chunk ([16 float4]
-// [128 heads], fp32), then holds that chunk's P (128 heads x 64 candidates,
-// BF16, K-major rows of 128 B in the 128-byte swizzle) as the A operand of PV.
+// recv[b] receives the peer's partial scores of a chunk ([16 float4][128
+// heads], fp32); p holds the chunk's P (128 heads x 64 candidates, BF16,
+// K-major rows of 128 B in the 128-byte swizzle), the A operand of PV.
 struct AttSmem {
     alignas(1024) uint8_t x[kXBuf][kXBytes];    // dequantised candidates, 128-byte swizzle
     alignas(1024) float4 recv[2][16 * kHeads];
+    alignas(1024) uint8_t p[kHeads * 128];
     alignas(128) uint8_t stage[kStages][kChunk * kSlot];
     uint64_t vmask[kStages], smask[kXBuf];
     uint64_t stg_full[kStages], stg_empty[kStages];
     uint64_t x_full[kXBuf], x_empty[kXBuf];
     uint64_t s_full[2], s_free[2], p_full[2], rd_done[2];
     uint64_t xchg_full[2], xchg_free[2];
-    uint64_t o_done, q_ready, mma_done;
+    uint64_t o_done[2], o_final, q_ready, mma_done;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -155,9 +156,9 @@ __device__ __forceinline__ void store_atom_row(uint8_t *xa, int row, const uint4
 //              PV(j) = P(j) X(j) -> O (after P(j) is ready); QK(j+2) is
 //              issued before PV(j), so scores run two chunks ahead
 //   softmax:   sends S(j+1) to the peer, combines S(j) with the peer's
-//              partial, releases S[j & 1], writes P(j) into recv[j & 1]
-//   PV(j) completion frees X[j % 3] and, by a multicast commit, tells the
-//   peer that it may write chunk j+2's partial into this CTA's recv[j & 1].
+//              partial, releases S[j & 1] and (to the peer) recv[j & 1],
+//              writes P(j) into the P buffer once PV(j-1) is done
+//   PV(j) completion frees X[j % 3] and the P buffer.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 attention_tc_kernel(const AttParams P) {
     extern __shared__ uint8_t smem_raw[];
@@ -183,9 +184,10 @@ attention_tc_kernel(const AttParams P) {
             ptx::mbar_init(&s.p_full[i], 4);
             ptx::mbar_init(&s.rd_done[i], 4);  // every softmax warp has read recv[i]
             ptx::mbar_init(&s.xchg_full[i], 1);  // local expect_tx + the peer's st.async bytes
-            ptx::mbar_init(&s.xchg_free[i], 1);  // the peer's multicast commit after its PV
+            ptx::mbar_init(&s.xchg_free[i], 1);  // the peer has read its recv[i]
+            ptx::mbar_init(&s.o_done[i], 1);     // PV of a chunk of this parity is done
         }
-        ptx::mbar_init(&s.o_done, 1);
+        ptx::mbar_init(&s.o_final, 1);
         ptx::mbar_init(&s.q_ready, 4);
         ptx::mbar_init(&s.mma_done, 1);
         s.abort_flag = 0;
@@ -308,15 +310,14 @@ attention_tc_kernel(const AttParams P) {
             ptx::tc_fence_after();
             if (lane == 0) {
                 const uint32_t xa = ptx::smem_u32(s.x[xb]);
-                const uint32_t pa = ptx::smem_u32(s.recv[pb]);
+                const uint32_t pa = ptx::smem_u32(s.p);
 #pragma unroll
                 for (int kk = 0; kk < kChunk / 16; ++kk)
                     ptx::mma_f16(tmem + kColO, ptx::desc_kmajor_sw128(pa + kk * 32),
                                  ptx::desc_mnmajor_sw128(xa + kk * 2048, kAtom, 1024), kIdescPV,
                                  (jp > 0 || kk > 0) ? 1u : 0u);
                 ptx::mma_commit(&s.x_empty[xb]);
-                ptx::mma_commit(&s.o_done);
-                ptx::mma_commit_multicast(&s.xchg_free[pb], static_cast<uint16_t>(1u << peer));
+                ptx::mma_commit(&s.o_done[pb]);
             }
             __syncwarp();
             return true;
@@ -327,7 +328,10 @@ attention_tc_kernel(const AttParams P) {
             if (j + 2 < u.n_chunks && !issue_qk(j + 2)) { fail(); ok = false; break; }
             if (!issue_pv(j)) { fail(); ok = false; break; }
         }
-        if (lane == 0) ptx::mma_commit(&s.mma_done);
+        if (lane == 0) {
+            ptx::mma_commit(&s.o_final);
+            ptx::mma_commit(&s.mma_done);
+        }
         __syncwarp();
         wait(&s.mma_done, 0);
     } else if (warp < 6) {
@@ -415,11 +419,13 @@ attention_tc_kernel(const AttParams P) {
                                        ptx::mapa(ptx::smem_u32(s.recv[1]), peer)};
         const uint32_t full_peer[2] = {ptx::mapa(ptx::smem_u32(&s.xchg_full[0]), peer),
                                        ptx::mapa(ptx::smem_u32(&s.xchg_full[1]), peer)};
+        const uint32_t free_peer[2] = {ptx::mapa(ptx::smem_u32(&s.xchg_free[0]), peer),
+                                       ptx::mapa(ptx::smem_u32(&s.xchg_free[1]), peer)};
         float m = -INFINITY, l = 0.f;  // running max and sum, log2 domain, sink not included
         // Sends this CTA's partial scores of chunk jj into the peer's recv
         // (st.async, completing bytes on the peer's xchg_full barrier) once the
-        // peer's PV(jj-2) has released that buffer, and arms the local receive
-        // barrier of chunk jj.
+        // peer has read chunk jj-2 out of that buffer, and arms the local
+        // receive barrier of chunk jj.
         auto send = [&](int jj) -> bool {
             const int b2 = jj & 1;
             if (!wait(&s.s_full[b2], (jj >> 1) & 1)) return false;
@@ -466,10 +472,11 @@ attention_tc_kernel(const AttParams P) {
                 z[4 * cq + 2] = __uint_as_float(own[2]) + pv.z;
                 z[4 * cq + 3] = __uint_as_float(own[3]) + pv.w;
             }
-            // every softmax thread has read recv[jb] before P overwrites it
+            // once every softmax thread has read recv[jb], the peer may refill it
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&s.rd_done[jb]);
             if (!wait(&s.rd_done[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
+            if (threadIdx.x == 192) ptx::mbar_arrive_remote(free_peer[jb]);
             if (!wait(&s.x_full[xb], (j / kXBuf) & 1)) { fail(); ok = false; break; }
             const uint64_t mask = s.smask[xb];
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -486,8 +493,10 @@ attention_tc_kernel(const AttParams P) {
             if (__any_sync(0xffffffffu, need)) {
                 const float alpha = need ? ptx::ex2_approx(m - mx) : 1.f;  // 0 when m = -inf
                 if (j > 0) {
-                    // O holds PV of chunks < j: wait for the last one, then rescale in place
-                    if (!wait(&s.o_done, (j - 1) & 1)) { fail(); ok = false; break; }
+                    // O holds PV of chunks < j: wait for the last one, then rescale in place.
+                    // (PV(j-3) is done -- it freed X for chunk j -- so this barrier is at
+                    // most one phase behind and the parity test is unambiguous.)
+                    if (!wait(&s.o_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) { fail(); ok = false; break; }
                     ptx::tc_fence_after();
 #pragma unroll 1
                     for (int piece = 0; piece < kHalf / 32; ++piece) {
@@ -504,10 +513,12 @@ attention_tc_kernel(const AttParams P) {
                 l *= alpha;
                 if (need) m = mx;
             }
-            // P(j) = 2^(z - m) as BF16 rows in recv[jb] (K-major, 128-byte swizzle)
+            // P(j) = 2^(z - m) as BF16 rows (K-major, 128-byte swizzle), once PV(j-1)
+            // has finished reading the previous P
+            if (j > 0 && !wait(&s.o_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) { fail(); ok = false; break; }
             const float mref = (m == -INFINITY) ? 0.f : m;  // every z is -inf while m is
             float ps4[4] = {0.f, 0.f, 0.f, 0.f};
-            uint8_t *prow = reinterpret_cast<uint8_t *>(s.recv[jb]) + h * 128;
+            uint8_t *prow = s.p + h * 128;
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) {
                 uint32_t w[4];
@@ -527,7 +538,7 @@ attention_tc_kernel(const AttParams P) {
         }
         // ---------------- epilogue: O half (and LSE) out
         if (ok && u.n_chunks > 0) {
-            if (!wait(&s.o_done, (u.n_chunks - 1) & 1)) { fail(); ok = false; }
+            if (!wait(&s.o_final, 0)) { fail(); ok = false; }
             ptx::tc_fence_after();
         }
         if (ok) {
