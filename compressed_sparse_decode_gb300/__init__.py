@@ -28,7 +28,8 @@ OP_INDEXER, OP_TOPK, OP_ATTENTION, OP_HCA_ATTENTION, OP_DECODE_STEP = range(5)
 
 EXPORTED = ["csa_workspace_bytes", "csa_indexer_logits", "csa_topk", "csa_gather_swa",
             "csa_sink_attention_decode", "hca_sink_attention_decode", "csa_decode_step",
-            "csa_read_device_error", "csa_status_string", "csa_version", "csa_kernel_launches"]
+            "csa_read_device_error", "csa_status_string", "csa_version", "csa_kernel_launches",
+            "csa_sink_attention_decode_noalloc"]
 
 
 class CsaError(RuntimeError):
@@ -80,6 +81,9 @@ def load(path: str | None = None):
         lib.csa_decode_step.argtypes = ([P] * 7 + [f32, csa_cache_desc, P, i32, i32, P, P] + [i32] * 5
                                         + [P, P, P, P, P, sz, P])
         lib.csa_decode_step.restype = st
+        lib.csa_sink_attention_decode_noalloc.argtypes = ([P, P, f32, csa_cache_desc, P, i32, i32, P, P, P, i32, i32,
+                                                           i32, P, P, P])
+        lib.csa_sink_attention_decode_noalloc.restype = st
         lib.csa_read_device_error.argtypes = [C.POINTER(C.c_int32), P]
         lib.csa_read_device_error.restype = st
         _lib = lib
@@ -233,6 +237,29 @@ def csa_sink_attention_decode(q, sink, softmax_scale: float, comp: csa_cache_des
         _ptr(out, "out", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(lse, "lse", torch.float32, (B, T, HEADS)),
         _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _stream(stream)),
         "csa_sink_attention_decode")
+    return out, lse
+
+
+def csa_sink_attention_decode_noalloc(q, sink, softmax_scale: float, comp: csa_cache_desc, swa_ring, W: int, topk_idx,
+                                      topk_cnt, q_pos, out=None, lse=None, stream=None):
+    """csa_sink_attention_decode without a workspace: for callers that cannot
+    allocate device memory on the decode path (see include/csa.h); the split
+    partials use the library's static device scratch."""
+    B, T = q_pos.shape
+    k = topk_idx.shape[2]
+    R = swa_ring.shape[1]
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, T, HEADS, DIM), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, T, HEADS), dtype=torch.float32, device=dev)
+    _check(load().csa_sink_attention_decode_noalloc(
+        _ptr(q, "q", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(sink, "sink", torch.float32, (HEADS,)),
+        float(softmax_scale), comp, _ptr(swa_ring, "swa_ring", torch.uint8, (B, R, RECORD_BYTES)), R, int(W),
+        _ptr(topk_idx, "topk_idx", torch.int32, (B, T, k)), _ptr(topk_cnt, "topk_cnt", torch.int32, (B, T)),
+        _ptr(q_pos, "q_pos", torch.int32, (B, T)), B, T, k,
+        _ptr(out, "out", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(lse, "lse", torch.float32, (B, T, HEADS)),
+        _stream(stream)), "csa_sink_attention_decode_noalloc")
     return out, lse
 
 

@@ -74,6 +74,11 @@ bool valid_dims(int B, int T) { return B >= 1 && T >= 1 && T <= CSA_MAX_TOKENS_P
 
 }  // namespace
 
+namespace csa {
+// Error word of the current device, for entry points defined in other files.
+int *error_word_for_current_device() { return device_error_word(); }
+}  // namespace csa
+
 extern "C" {
 
 int csa_version(void) { return 100; }

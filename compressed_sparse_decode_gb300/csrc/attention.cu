@@ -30,6 +30,8 @@
 // combine kernel folds the splits and the sink. Every wait is bounded.
 #include <cuda.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -718,4 +720,72 @@ cudaError_t launch_attention(const void *q, const float *sink, float scale, cons
     return cudaGetLastError();
 }
 
+int *error_word_for_current_device();
+
+// ------------------------------------------------------------------ allocation-free variant
+//
+// Some callers of this library cannot allocate device memory on the decode
+// path, so they cannot provide the split partials' workspace either: a serving
+// runtime whose whole device memory is reserved by its own pool at start-up, a
+// plugin inside a host framework that owns every device allocation, or host
+// code on a latency-critical path where cudaMalloc's implicit device-wide
+// synchronisation is not acceptable. For them, csa_sink_attention_decode_noalloc
+// runs the same attention with its scratch in the static array below.
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB, held by every device that loads the library
+__device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+void *g_static_scratch_addr[kMaxDevices];
+std::mutex g_static_scratch_mu;
+
+// Device address of the static scratch on the current device. In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+cudaError_t static_scratch_address(void **addr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+    if (!g_static_scratch_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return e;
+        g_static_scratch_addr[dev] = p;
+    }
+    *addr = g_static_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
 }  // namespace csa
+
+extern "C" CSA_API csa_status_t csa_sink_attention_decode_noalloc(
+    const void *q, const float *sink, float softmax_scale, csa_cache_desc comp, const void *swa_ring, int R, int W,
+    const int32_t *topk_idx, const int32_t *topk_cnt, const int32_t *q_pos, int B, int T, int k, void *out, float *lse,
+    cudaStream_t stream) {
+    using namespace csa;
+    const auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!q || !sink || !swa_ring || !topk_idx || !topk_cnt || !q_pos || !out || !lse) return CSA_ERR_INVALID_ARG;
+    if (!a16(q) || !a16(swa_ring) || !a16(out) || !comp.base || !a16(comp.base) || comp.n_records <= 0 ||
+        comp.seq_capacity <= 0)
+        return CSA_ERR_INVALID_ARG;
+    if (comp.block_table ? (!a16(comp.block_table) || comp.page_records <= 0 || comp.max_pages <= 0)
+                         : (comp.seq_stride < 0 || (B > 1 && comp.seq_stride < comp.seq_capacity)))
+        return CSA_ERR_INVALID_ARG;
+    if (B < 1 || T < 1 || T > CSA_MAX_TOKENS_PER_SEQ || (int64_t)B * T > 65535 || k < 1 || W < 1 ||
+        W > CSA_MAX_SWA_WINDOW || R < W || !(softmax_scale > 0.f))
+        return CSA_ERR_INVALID_ARG;
+    if (k > CSA_MAX_TOPK) return CSA_ERR_UNSUPPORTED;
+    const size_t need = attention_workspace_bytes(B, T, k + CSA_MAX_SWA_WINDOW);
+    if (need > kStaticScratchBytes) return CSA_ERR_UNSUPPORTED;  // beyond the static scratch: use the workspace call
+    void *scratch = nullptr;
+    if (need && static_scratch_address(&scratch) != cudaSuccess) return CSA_ERR_CUDA;
+    const cudaError_t e = launch_attention(q, sink, softmax_scale, comp, swa_ring, R, W, topk_idx, topk_cnt, nullptr,
+                                           1, q_pos, B, T, k, false, k + CSA_MAX_SWA_WINDOW, out, lse, scratch,
+                                           need ? kStaticScratchBytes : 0, error_word_for_current_device(), stream);
+    return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
+}

@@ -186,6 +186,31 @@ CSA_API csa_status_t hca_sink_attention_decode(const void *q, const float *sink,
                                        int B, int T, int m_hca, void *out, float *lse,
                                        void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Allocation-free variant of csa_sink_attention_decode (the pages have no
+ * counterpart; it exists for callers of this library that cannot allocate
+ * device memory on the decode path -- e.g. a serving runtime whose device
+ * memory is all reserved by its own pool at start-up, a plugin whose host
+ * framework owns every device allocation, or latency-critical host code that
+ * cannot afford cudaMalloc's implicit synchronisation -- and so cannot pass a
+ * workspace). Same arguments and results as csa_sink_attention_decode minus
+ * the workspace: the split partials live in a static 16 MiB device array that
+ * every device which loads the library holds until the process exits.
+ *  - No cudaMalloc, cudaFree or allocating library call is made.
+ *  - The first call on a device (with that device current) looks up the
+ *    array's device address once (cudaGetSymbolAddress) and caches it; make
+ *    that first call before any stream capture.
+ *  - Sizes whose partials exceed the array return CSA_ERR_UNSUPPORTED (use
+ *    csa_sink_attention_decode with a workspace instead); the limit is
+ *    csa_workspace_bytes(CSA_OP_ATTENTION, B, T, Ncap, k) <= 16 MiB.
+ *  - Every call shares the array and leaves its contents behind; nothing in it
+ *    needs to start at zero. Calls that overlap on the GPU (concurrent streams)
+ *    race on the array: serialise them. */
+CSA_API csa_status_t csa_sink_attention_decode_noalloc(const void *q, const float *sink, float softmax_scale,
+                                                       csa_cache_desc comp, const void *swa_ring, int R, int W,
+                                                       const int32_t *topk_idx, const int32_t *topk_cnt,
+                                                       const int32_t *q_pos, int B, int T, int k, void *out,
+                                                       float *lse, cudaStream_t stream);
+
 /* One CSA decode step: csa_indexer_logits -> csa_topk ->
  * csa_sink_attention_decode on one stream. Logits, indices and attention
  * scratch live in the workspace (csa_workspace_bytes(CSA_OP_DECODE_STEP,...)).
