@@ -8,16 +8,18 @@
 // which is the weighted-ReLU form because the FP8 scales are positive. Entries
 // c >= n_vis(b,t) get -inf ("DSV4 Audit", section A3, item 1).
 //
-// Design (one persistent CTA per SM, 6 warps):
+// Design (one persistent CTA per SM, 10 warps):
 //   warp 0   TMA producer: 128-key x 128-byte FP8 tiles (128-byte swizzle) into
 //            an 8-stage shared-memory ring; per sequence, the T*64 query rows
 //            (FP8) and the head weights w*sq into one of two query slots.
 //   warp 1   MMA issuer: tcgen05.mma kind::f8f6f4, M = 128 keys, N = 64*T
 //            query-head rows, K = 128 (4 x K32), fp32 accumulator in TMEM,
 //            two accumulator buffers so the epilogue overlaps the next tile.
-//   warps 2-5 epilogue: thread i owns TMEM lane i = key c0+i; it reads the
-//            64*T head dot products, applies ReLU and the head weights, scales
-//            by the key's scale and writes the row of logits (coalesced).
+//   warps 2-9 epilogue, two groups of 4 taking alternate tiles: thread i owns
+//            TMEM lane i = key c0+i; it reads the 64*T head dot products,
+//            applies ReLU and the head weights, scales by the key's scale and
+//            writes the row of logits (coalesced). Up to four accumulator
+//            buffers let the MMA run ahead of both groups.
 // Keys are read once from HBM for all T tokens of a sequence; tiles past the
 // largest visible range of their sequence are never loaded (written -inf).
 // Every wait is bounded; a timeout records CSA_ERR_TIMEOUT and the CTA exits
@@ -34,7 +36,7 @@ namespace {
 constexpr int kTileKeys = 128;
 constexpr int kStages = 8;
 constexpr int kTileBytes = kTileKeys * kIdxDim;  // 16 KB
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA, two 4-warp epilogue groups
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
 template <int T>
@@ -44,7 +46,7 @@ struct IdxSmem {
     alignas(1024) uint8_t q[2][kQBytes];
     float ws[2][T * kIdxHeads];  // w * sq per query slot
     uint64_t full[kStages], empty[kStages];
-    uint64_t acc_full[2], acc_empty[2];
+    uint64_t acc_full[4], acc_empty[4];
     uint64_t q_full[2], q_empty[2];
     uint64_t mma_done;
     uint32_t tmem_base;
@@ -71,7 +73,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                   const float *__restrict__ k_scale, const int32_t *__restrict__ q_pos,
                   const int32_t *__restrict__ n_comp, int B, int Ncap, int m, float *__restrict__ logits, int *err) {
     constexpr int N = T * kIdxHeads;
-    constexpr uint32_t kTmemCols = (2 * N <= 128) ? 128 : (2 * N <= 256 ? 256 : 512);
+    constexpr int kAcc = (4 * N <= 512) ? 4 : 2;  // TMEM accumulator buffers
+    constexpr uint32_t kTmemCols = (kAcc * N <= 128) ? 128 : (kAcc * N <= 256 ? 256 : 512);
     constexpr uint32_t kIdesc = ptx::idesc_f32acc(0, 0, kTileKeys, N);
     extern __shared__ uint8_t smem_raw[];
     IdxSmem<T> &s = *reinterpret_cast<IdxSmem<T> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -88,11 +91,13 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             ptx::mbar_init(&s.full[i], 1);
             ptx::mbar_init(&s.empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4; ++i) {
             ptx::mbar_init(&s.acc_full[i], 1);
             ptx::mbar_init(&s.acc_empty[i], 4);
+        }
+        for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&s.q_full[i], 1 + 32);
-            ptx::mbar_init(&s.q_empty[i], 1 + 4);
+            ptx::mbar_init(&s.q_empty[i], 1 + 8);
         }
         ptx::mbar_init(&s.mma_done, 1);
         s.abort_flag = 0;
@@ -180,8 +185,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 ++u;
             }
             const int st = j % kStages;
-            const int buf = a & 1;
-            if (!wait(&s.acc_empty[buf], ((a >> 1) & 1) ^ 1)) { fail(); ok = false; break; }
+            const int buf = a % kAcc;
+            if (!wait(&s.acc_empty[buf], ((a / kAcc) & 1) ^ 1)) { fail(); ok = false; break; }
             if (!wait(&s.full[st], (j / kStages) & 1)) { fail(); ok = false; break; }
             ptx::tc_fence_after();
             if (lane == 0) {
@@ -206,30 +211,41 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         wait(&s.mma_done, 0);
     } else {
         // ------------------------------------------------------------ epilogue
+        // Two groups of 4 warps take alternate accumulated tiles (group g owns
+        // the non-skipped tiles whose ordinal a has a & 1 == g); skipped tiles
+        // are written by the group of their tile index parity.
+        const int group = (warp - 2) >> 2;
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const int row = quarter * 32 + lane;
         int cb = -1, cnv = 0, active_b = -1;
-        int pb = -1, pnv = 0;  // visibility cache of the prefetch walk
         uint32_t u = 0, a = 0;
         int nvis[T];
-        // key scales are fetched one tile ahead so that their HBM latency
-        // overlaps the current tile instead of stalling it
-        auto fetch_scale = [&](long i) -> float {
-            if (i >= t_end) return 0.f;
-            const TileInfo ti = tile_at(i, pb, pnv);
-            const int c = ti.c0 + row;
-            return (!ti.skip && c < Ncap) ? __ldg(k_scale + (size_t)ti.b * Ncap + c) : 0.f;
+        // key scales of the group's next own tile are fetched while the
+        // current one is processed (their HBM latency overlaps two tiles)
+        int pb = -1, pnv = 0;
+        long pi = t_begin;
+        uint32_t pa = 0;
+        auto fetch_next_own = [&]() -> float {
+            while (pi < t_end) {
+                const TileInfo ti = tile_at(pi, pb, pnv);
+                ++pi;
+                if (ti.skip) continue;
+                const bool own = (pa & 1u) == (uint32_t)group;
+                ++pa;
+                if (!own) continue;
+                const int c = ti.c0 + row;
+                return c < Ncap ? __ldg(k_scale + (size_t)ti.b * Ncap + c) : 0.f;
+            }
+            return 0.f;
         };
-        float sk_next = fetch_scale(t_begin);
+        float sk_next = fetch_next_own();
         bool ok = true;
         for (long i = t_begin; i < t_end && ok; ++i) {
             const TileInfo ti = tile_at(i, cb, cnv);
-            const float sk = sk_next;
-            sk_next = fetch_scale(i + 1);
             const int c = ti.c0 + row;
             float *lrow = logits + (size_t)ti.b * T * Ncap + c;
             if (ti.skip) {
-                if (c < Ncap)
+                if ((i & 1) == group && c < Ncap)
                     for (int t = 0; t < T; ++t) lrow[(size_t)t * Ncap] = -INFINITY;
                 continue;
             }
@@ -241,8 +257,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     nvis[t] = visible_entries(__ldg(q_pos + ti.b * T + t), m, __ldg(n_comp + ti.b), Ncap);
                 ++u;
             }
-            const int buf = a & 1;
-            if (!wait(&s.acc_full[buf], (a >> 1) & 1)) { fail(); ok = false; break; }
+            const uint32_t my_a = a++;
+            if ((my_a & 1u) != (uint32_t)group) continue;
+            const float sk = sk_next;
+            sk_next = fetch_next_own();
+            const int buf = my_a % kAcc;
+            if (!wait(&s.acc_full[buf], (my_a / kAcc) & 1)) { fail(); ok = false; break; }
             ptx::tc_fence_after();
             const float *ws = s.ws[(u - 1) & 1];
             float acc[T];
@@ -254,20 +274,20 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 ptx::tmem_ld32(col + 32, r1);
                 ptx::tmem_ld_wait();
                 const float4 *w4 = reinterpret_cast<const float4 *>(ws + t * kIdxHeads);
-                float s0 = 0.f, s1 = 0.f;
+                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
                 for (int h4 = 0; h4 < 8; ++h4) {
                     const float4 wa = w4[h4], wb = w4[8 + h4];
                     s0 = fmaf(wa.x, fmaxf(__uint_as_float(r0[4 * h4 + 0]), 0.f), s0);
-                    s0 = fmaf(wa.y, fmaxf(__uint_as_float(r0[4 * h4 + 1]), 0.f), s0);
+                    s1 = fmaf(wa.y, fmaxf(__uint_as_float(r0[4 * h4 + 1]), 0.f), s1);
                     s0 = fmaf(wa.z, fmaxf(__uint_as_float(r0[4 * h4 + 2]), 0.f), s0);
-                    s0 = fmaf(wa.w, fmaxf(__uint_as_float(r0[4 * h4 + 3]), 0.f), s0);
-                    s1 = fmaf(wb.x, fmaxf(__uint_as_float(r1[4 * h4 + 0]), 0.f), s1);
-                    s1 = fmaf(wb.y, fmaxf(__uint_as_float(r1[4 * h4 + 1]), 0.f), s1);
-                    s1 = fmaf(wb.z, fmaxf(__uint_as_float(r1[4 * h4 + 2]), 0.f), s1);
-                    s1 = fmaf(wb.w, fmaxf(__uint_as_float(r1[4 * h4 + 3]), 0.f), s1);
+                    s1 = fmaf(wa.w, fmaxf(__uint_as_float(r0[4 * h4 + 3]), 0.f), s1);
+                    s2 = fmaf(wb.x, fmaxf(__uint_as_float(r1[4 * h4 + 0]), 0.f), s2);
+                    s3 = fmaf(wb.y, fmaxf(__uint_as_float(r1[4 * h4 + 1]), 0.f), s3);
+                    s2 = fmaf(wb.z, fmaxf(__uint_as_float(r1[4 * h4 + 2]), 0.f), s2);
+                    s3 = fmaf(wb.w, fmaxf(__uint_as_float(r1[4 * h4 + 3]), 0.f), s3);
                 }
-                acc[t] = s0 + s1;
+                acc[t] = (s0 + s1) + (s2 + s3);
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -276,7 +296,6 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 #pragma unroll
                 for (int t = 0; t < T; ++t) lrow[(size_t)t * Ncap] = c < nvis[t] ? acc[t] * sk : -INFINITY;
             }
-            ++a;
         }
         if (ok && active_b >= 0 && lane == 0) ptx::mbar_arrive(&s.q_empty[(u - 1) & 1]);
     }

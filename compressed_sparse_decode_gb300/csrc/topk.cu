@@ -29,7 +29,8 @@ constexpr int kMaxResident = 32768;      // keys per CTA held in shared memory
 struct TopkShared {
     uint32_t merged[3][kBins];  // rank 0's copy receives every CTA's histogram, one buffer per pass
     uint32_t local[kBins];      // this CTA's histogram of the current pass
-    int counts[kCtas][2];       // rank 0's copy: (keys > K*, keys == K*) per CTA
+    alignas(16) uint32_t view[kBins];  // local copy of the merged histogram of the current pass
+    alignas(16) int counts[kCtas][2];  // rank 0's copy: (keys > K*, keys == K*) per CTA
     int scan[kWarps + 1];
     int wsum[2][kWarps];
     uint32_t digit;
@@ -61,9 +62,10 @@ __device__ __forceinline__ int block_exclusive_scan(int flag, int *s_warp, int &
     return res;
 }
 
-__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+__device__ __forceinline__ uint4 ld_cluster_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr) : "memory");
     return v;
 }
 
@@ -139,12 +141,15 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
             s.local[d] = 0u;
         }
         ptx::cluster_sync();
-        // every CTA reads the merged histogram and picks the same digit
+        // every CTA copies the merged histogram (one vector load per thread)
+        // and picks the same digit from its local copy
+        for (int v = tid; v < kBins / 4; v += kThreads)
+            reinterpret_cast<uint4 *>(s.view)[v] = ld_cluster_v4(merged0 + (uint32_t)((pass * kBins + 4 * v) * 4));
+        __syncthreads();
         if (warp == 0) {
             const int nb = (int)dmask + 1, per = nb / 32;  // bins per lane, descending digits
             int sum = 0;
-            for (int j = 0; j < per; ++j)
-                sum += (int)ld_cluster_u32(merged0 + (uint32_t)((pass * kBins + (nb - 1 - (lane * per + j))) * 4));
+            for (int j = 0; j < per; ++j) sum += (int)s.view[nb - 1 - (lane * per + j)];
             int incl = sum;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -157,7 +162,7 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
                 int cum = excl;
                 for (int j = 0; j < per; ++j) {
                     const int d = nb - 1 - (lane * per + j);
-                    const int c = (int)ld_cluster_u32(merged0 + (uint32_t)((pass * kBins + d) * 4));
+                    const int c = (int)s.view[d];
                     if (cum + c >= remaining) {
                         s.digit = (uint32_t)d;
                         s.remaining = remaining - cum;
@@ -203,10 +208,12 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
         st_cluster_s32(counts0 + crank * 8 + 4, tot_eq);
     }
     ptx::cluster_sync();
+    if (tid < kCtas * 2 / 4) reinterpret_cast<uint4 *>(s.view)[tid] = ld_cluster_v4(counts0 + tid * 16);
+    __syncthreads();
     int base = 0, eq_before = 0;
     for (int c = 0; c < (int)crank; ++c) {
-        const int cg = (int)ld_cluster_u32(counts0 + c * 8);
-        const int ce = (int)ld_cluster_u32(counts0 + c * 8 + 4);
+        const int cg = (int)s.view[2 * c];
+        const int ce = (int)s.view[2 * c + 1];
         const int take_eq = min(max(remaining - eq_before, 0), ce);
         base += cg + take_eq;
         eq_before += ce;
