@@ -6,13 +6,14 @@
 // [c * slice, (c + 1) * slice) of the row. Each CTA loads its slice once into
 // shared memory as order-preserving 32-bit keys, then a radix select finds the
 // k-th largest key K* in three digit passes (bits 31..21, 20..10, 9..0):
-// per pass, every CTA builds a histogram of its matching keys (warp-aggregated
-// with __match_any_sync), adds it into rank 0's copy through distributed shared
-// memory, and after a cluster barrier every CTA reads the merged histogram and
-// picks the same digit. Finally each CTA keeps its keys > K* and, in index
-// order, the lowest-index keys == K* still needed; the per-CTA counts are
-// exchanged through rank 0 so every CTA writes at its global offset and the
-// output is in ascending index order. No lock and no global atomic is used.
+// per pass, every CTA builds a histogram of its matching keys in its own
+// shared memory (warp-aggregated with __match_any_sync); after a cluster
+// barrier each thread sums its bins over the 8 CTAs through distributed shared
+// memory, and every CTA picks the same digit. Finally each CTA keeps its keys
+// > K* and, in index order, the lowest-index keys == K* still needed; the
+// per-CTA counts are exchanged through rank 0 so every CTA writes at its
+// global offset and the output is in ascending index order. No lock and no
+// global atomic is used.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -27,9 +28,8 @@ constexpr int kBins = 2048;              // 11-bit digits (the last pass uses 10
 constexpr int kMaxResident = 32768;      // keys per CTA held in shared memory
 
 struct TopkShared {
-    uint32_t merged[3][kBins];  // rank 0's copy receives every CTA's histogram, one buffer per pass
-    uint32_t local[kBins];      // this CTA's histogram of the current pass
-    alignas(16) uint32_t view[kBins];  // local copy of the merged histogram of the current pass
+    alignas(16) uint32_t local[3][kBins];  // this CTA's histogram, one buffer per pass (read by every CTA)
+    alignas(16) uint32_t view[kBins];      // the cluster-wide histogram of the current pass
     alignas(16) int counts[kCtas][2];  // rank 0's copy: (keys > K*, keys == K*) per CTA
     int scan[kWarps + 1];
     int wsum[2][kWarps];
@@ -69,10 +69,6 @@ __device__ __forceinline__ uint4 ld_cluster_v4(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ void red_cluster_add(uint32_t addr, uint32_t v) {
-    asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
     asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
@@ -107,13 +103,9 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
     };
     if (resident)
         for (int i = lo + tid; i < hi; i += kThreads) keys[i - lo] = order_key(__ldg(row + i));
-    for (int i = tid; i < 3 * kBins; i += kThreads) (&s.merged[0][0])[i] = 0u;
-    for (int i = tid; i < kBins; i += kThreads) s.local[i] = 0u;
-    if (tid < kCtas * 2) (&s.counts[0][0])[tid] = 0;
+    for (int i = tid; i < 3 * kBins; i += kThreads) (&s.local[0][0])[i] = 0u;
     __syncthreads();
-    ptx::cluster_sync();  // rank 0's merge buffers are zero before anyone adds into them
 
-    const uint32_t merged0 = ptx::mapa(ptx::smem_u32(&s.merged[0][0]), 0);
     uint32_t prefix = 0, mask = 0;
     int remaining = k;
 #pragma unroll 1
@@ -130,21 +122,25 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
             if (match) {
                 const uint32_t d = (key >> shift) & dmask;
                 const unsigned peers = __match_any_sync(act, d);
-                if (lane == __ffs(peers) - 1) atomicAdd(&s.local[d], (uint32_t)__popc(peers));
+                if (lane == __ffs(peers) - 1) atomicAdd(&s.local[pass][d], (uint32_t)__popc(peers));
             }
         }
-        __syncthreads();
-        // add it into rank 0's merge buffer for this pass, then clear it
-        for (int d = tid; d <= (int)dmask; d += kThreads) {
-            const uint32_t v = s.local[d];
-            if (v) red_cluster_add(merged0 + (uint32_t)((pass * kBins + d) * 4), v);
-            s.local[d] = 0u;
+        ptx::cluster_sync();  // every CTA's histogram of this pass is complete
+        // the cluster-wide histogram: each thread sums 4 bins over the 8 CTAs
+        // (one vector load of distributed shared memory per CTA)
+        if (tid < (int)(dmask + 1) / 4) {
+            const uint32_t off = ptx::smem_u32(&s.local[pass][4 * tid]);
+            uint4 acc = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int c = 0; c < kCtas; ++c) {
+                const uint4 v = ld_cluster_v4(ptx::mapa(off, c));
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            reinterpret_cast<uint4 *>(s.view)[tid] = acc;
         }
-        ptx::cluster_sync();
-        // every CTA copies the merged histogram (one vector load per thread)
-        // and picks the same digit from its local copy
-        for (int v = tid; v < kBins / 4; v += kThreads)
-            reinterpret_cast<uint4 *>(s.view)[v] = ld_cluster_v4(merged0 + (uint32_t)((pass * kBins + 4 * v) * 4));
         __syncthreads();
         if (warp == 0) {
             const int nb = (int)dmask + 1, per = nb / 32;  // bins per lane, descending digits
