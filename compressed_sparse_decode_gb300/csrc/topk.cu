@@ -3,17 +3,20 @@
 // warp-level reductions and no global lock).
 //
 // One row (query token) per cluster of 8 CTAs; CTA rank c owns the slice
-// [c * slice, (c + 1) * slice) of the row. Each CTA loads its slice once into
-// shared memory as order-preserving 32-bit keys, then a radix select finds the
-// k-th largest key K* in three digit passes (bits 31..21, 20..10, 9..0):
-// per pass, every CTA builds a histogram of its matching keys in its own
-// shared memory (warp-aggregated with __match_any_sync); after a cluster
-// barrier each thread sums its bins over the 8 CTAs through distributed shared
-// memory, and every CTA picks the same digit. Finally each CTA keeps its keys
-// > K* and, in index order, the lowest-index keys == K* still needed; the
-// per-CTA counts are exchanged through rank 0 so every CTA writes at its
-// global offset and the output is in ascending index order. No lock and no
-// global atomic is used.
+// [c * slice, (c + 1) * slice) of the row, and thread t of a CTA owns the
+// contiguous run of E = slice / 512 entries starting at t * E (kept in shared
+// memory transposed, keys[j][t], so every access is conflict-free). The CTA
+// loads its slice once as order-preserving 32-bit keys; a radix select then
+// finds the k-th largest key K* in three digit passes (bits 31..21, 20..10,
+// 9..0): per pass every CTA builds a histogram of its matching keys in its own
+// shared memory, and after a cluster barrier each thread sums 4 bins over the
+// 8 CTAs through distributed shared memory; a block-wide scan over the bins
+// (largest digit first) picks the digit, identically in every CTA. Finally
+// each CTA keeps its keys > K* and, in index order, the lowest-index keys ==
+// K* still needed: per-thread counts are scanned, the per-CTA totals are
+// exchanged through rank 0, and every thread writes its run at its global
+// offset, so the output is in ascending index order. No lock and no global
+// atomic is used.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -25,47 +28,44 @@ constexpr int kCtas = 8;                 // CTAs per row (a portable cluster)
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;              // 11-bit digits (the last pass uses 10)
-constexpr int kMaxResident = 32768;      // keys per CTA held in shared memory
+constexpr int kMaxRun = 64;             // entries per thread held in shared memory
 
 struct TopkShared {
     alignas(16) uint32_t local[3][kBins];  // this CTA's histogram, one buffer per pass (read by every CTA)
-    alignas(16) uint32_t view[kBins];      // the cluster-wide histogram of the current pass
-    alignas(16) int counts[kCtas][2];  // rank 0's copy: (keys > K*, keys == K*) per CTA
-    int scan[kWarps + 1];
-    int wsum[2][kWarps];
+    alignas(16) int counts[kCtas][2];      // rank 0's copy: (keys > K*, keys == K*) per CTA
+    alignas(16) int peer_counts[kCtas][2];
+    int wsum[kWarps];
     uint32_t digit;
     int remaining;
 };
 
-// Block-wide exclusive prefix sum of a 0/1 flag; every thread must call it.
-__device__ __forceinline__ int block_exclusive_scan(int flag, int *s_warp, int &total) {
+// Block-wide exclusive prefix sum of an int; every thread must call it.
+__device__ __forceinline__ int block_exclusive_sum(int v, int *wsum, int &total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned bal = __ballot_sync(0xffffffffu, flag);
-    const int rank = __popc(bal & ((1u << lane) - 1u));
-    if (lane == 0) s_warp[warp] = __popc(bal);
-    __syncthreads();
-    if (warp == 0) {
-        const int v = lane < kWarps ? s_warp[lane] : 0;
-        int incl = v;
+    int incl = v;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += u;
-        }
-        if (lane < kWarps) s_warp[lane] = incl - v;
-        if (lane == 31) s_warp[kWarps] = incl;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const int x = wsum[w];
+        before += w < warp ? x : 0;
+        all += x;
     }
     __syncthreads();
-    const int res = s_warp[warp] + rank;
-    total = s_warp[kWarps];
-    __syncthreads();
-    return res;
+    total = all;
+    return before + incl - v;
 }
 
 __device__ __forceinline__ uint4 ld_cluster_v4(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr) : "memory");
+                 : "r"(addr));
     return v;
 }
 
@@ -75,12 +75,12 @@ __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
 
 __global__ void __launch_bounds__(kThreads)
 topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict__ q_pos,
-                    const int32_t *__restrict__ n_comp, int T, int Ncap, int m, int k, int slice, int resident,
+                    const int32_t *__restrict__ n_comp, int T, int Ncap, int m, int k, int run, int resident,
                     int32_t *__restrict__ idx_out, int32_t *__restrict__ cnt_out) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     TopkShared &s = *reinterpret_cast<TopkShared *>(smem_raw);
-    uint32_t *keys = reinterpret_cast<uint32_t *>(smem_raw + sizeof(TopkShared));
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t *keys = reinterpret_cast<uint32_t *>(smem_raw + sizeof(TopkShared));  // [run][kThreads]
+    const int tid = threadIdx.x;
     const uint32_t crank = ptx::cluster_ctarank();
     const int r = blockIdx.x / kCtas;
     const int b = r / T;
@@ -96,13 +96,14 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
         return;  // uniform over the cluster: no shared memory of another CTA is touched
     }
 
-    const int lo = crank * slice;
-    const int hi = min(nv, lo + slice);
-    auto key_at = [&](int i) -> uint32_t {  // i in [lo, hi)
-        return resident ? keys[i - lo] : order_key(__ldg(row + i));
+    const int slice = run * kThreads;
+    const int mine = crank * slice + tid * run;  // first entry of this thread's run
+    const int n_my = max(0, min(run, nv - mine));
+    auto key_j = [&](int j) -> uint32_t {
+        return resident ? keys[j * kThreads + tid] : order_key(__ldg(row + mine + j));
     };
     if (resident)
-        for (int i = lo + tid; i < hi; i += kThreads) keys[i - lo] = order_key(__ldg(row + i));
+        for (int j = 0; j < n_my; ++j) keys[j * kThreads + tid] = order_key(__ldg(row + mine + j));
     for (int i = tid; i < 3 * kBins; i += kThreads) (&s.local[0][0])[i] = 0u;
     __syncthreads();
 
@@ -112,121 +113,94 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
     for (int pass = 0; pass < 3; ++pass) {
         const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);  // digits: bits 31..21, 20..10, 9..0
         const uint32_t dmask = pass == 2 ? 0x3FFu : 0x7FFu;
-        // local histogram of keys matching the digits chosen so far
-        for (int base = lo; base < hi; base += kThreads) {
-            const int i = base + tid;
-            const bool in = i < hi;
-            const uint32_t key = in ? key_at(i) : 0u;
-            const bool match = in && (key & mask) == prefix;
-            const unsigned act = __ballot_sync(0xffffffffu, match);
-            if (match) {
-                const uint32_t d = (key >> shift) & dmask;
-                const unsigned peers = __match_any_sync(act, d);
-                if (lane == __ffs(peers) - 1) atomicAdd(&s.local[pass][d], (uint32_t)__popc(peers));
-            }
+        for (int j = 0; j < n_my; ++j) {
+            const uint32_t key = key_j(j);
+            if ((key & mask) == prefix) atomicAdd(&s.local[pass][(key >> shift) & dmask], 1u);
         }
         ptx::cluster_sync();  // every CTA's histogram of this pass is complete
-        // the cluster-wide histogram: each thread sums 4 bins over the 8 CTAs
-        // (one vector load of distributed shared memory per CTA)
-        if (tid < (int)(dmask + 1) / 4) {
-            const uint32_t off = ptx::smem_u32(&s.local[pass][4 * tid]);
+        // Thread t sums bins [d0, d0+4) over the 8 CTAs (one vector load of
+        // distributed shared memory each); threads take the bins from the
+        // largest digit down, so a block-wide scan finds the digit that holds
+        // the `remaining`-th largest matching key.
+        const int nb = (int)dmask + 1;
+        int c4[4] = {0, 0, 0, 0};
+        int tsum = 0, d0 = 0;
+        if (tid < nb / 4) {
+            d0 = nb - 4 * (tid + 1);
+            const uint32_t off = ptx::smem_u32(&s.local[pass][d0]);
+            uint4 v[kCtas];
+#pragma unroll
+            for (int c = 0; c < kCtas; ++c) v[c] = ld_cluster_v4(ptx::mapa(off, c));
             uint4 acc = make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int c = 0; c < kCtas; ++c) {
-                const uint4 v = ld_cluster_v4(ptx::mapa(off, c));
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
+                acc.x += v[c].x;
+                acc.y += v[c].y;
+                acc.z += v[c].z;
+                acc.w += v[c].w;
             }
-            reinterpret_cast<uint4 *>(s.view)[tid] = acc;
+            c4[0] = (int)acc.w;  // digit d0 + 3
+            c4[1] = (int)acc.z;
+            c4[2] = (int)acc.y;
+            c4[3] = (int)acc.x;  // digit d0
+            tsum = c4[0] + c4[1] + c4[2] + c4[3];
         }
-        __syncthreads();
-        if (warp == 0) {
-            const int nb = (int)dmask + 1, per = nb / 32;  // bins per lane, descending digits
-            int sum = 0;
-            for (int j = 0; j < per; ++j) sum += (int)s.view[nb - 1 - (lane * per + j)];
-            int incl = sum;
+        int total;
+        const int excl = block_exclusive_sum(tsum, s.wsum, total);
+        if (tsum > 0 && excl < remaining && remaining <= excl + tsum) {
+            int cum = excl;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += u;
-            }
-            const int excl = incl - sum;
-            const unsigned here = __ballot_sync(0xffffffffu, excl < remaining && remaining <= incl);
-            if (lane == __ffs(here) - 1) {
-                int cum = excl;
-                for (int j = 0; j < per; ++j) {
-                    const int d = nb - 1 - (lane * per + j);
-                    const int c = (int)s.view[d];
-                    if (cum + c >= remaining) {
-                        s.digit = (uint32_t)d;
-                        s.remaining = remaining - cum;
-                        break;
-                    }
-                    cum += c;
+            for (int q = 0; q < 4; ++q) {
+                if (cum + c4[q] >= remaining) {
+                    s.digit = (uint32_t)(d0 + 3 - q);
+                    s.remaining = remaining - cum;
+                    break;
                 }
+                cum += c4[q];
             }
         }
         __syncthreads();
         prefix |= s.digit << shift;
         mask |= dmask << shift;
         remaining = s.remaining;
-        __syncthreads();
     }
 
-    // prefix = K*; keep every key > K* and the first `remaining` keys == K* (index order)
+    // prefix = K*: keep every key > K* and the first `remaining` keys == K* in index order
     int gt = 0, eq = 0;
-    for (int i = lo + tid; i < hi; i += kThreads) {
-        const uint32_t key = key_at(i);
+    for (int j = 0; j < n_my; ++j) {
+        const uint32_t key = key_j(j);
         gt += key > prefix;
         eq += key == prefix;
     }
-    // block totals of both counts
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        gt += __shfl_xor_sync(0xffffffffu, gt, o);
-        eq += __shfl_xor_sync(0xffffffffu, eq, o);
-    }
-    if (lane == 0) {
-        s.wsum[0][warp] = gt;
-        s.wsum[1][warp] = eq;
-    }
-    __syncthreads();
-    int tot_gt = 0, tot_eq = 0;
-    for (int w = 0; w < kWarps; ++w) {
-        tot_gt += s.wsum[0][w];
-        tot_eq += s.wsum[1][w];
-    }
+    int tot_gt, tot_eq;
+    block_exclusive_sum(gt, s.wsum, tot_gt);
+    const int eq_excl = block_exclusive_sum(eq, s.wsum, tot_eq);
     const uint32_t counts0 = ptx::mapa(ptx::smem_u32(&s.counts[0][0]), 0);
     if (tid == 0) {
         st_cluster_s32(counts0 + crank * 8, tot_gt);
         st_cluster_s32(counts0 + crank * 8 + 4, tot_eq);
     }
     ptx::cluster_sync();
-    if (tid < kCtas * 2 / 4) reinterpret_cast<uint4 *>(s.view)[tid] = ld_cluster_v4(counts0 + tid * 16);
+    if (tid < kCtas * 2 / 4) reinterpret_cast<uint4 *>(&s.peer_counts[0][0])[tid] = ld_cluster_v4(counts0 + tid * 16);
     __syncthreads();
     int base = 0, eq_before = 0;
     for (int c = 0; c < (int)crank; ++c) {
-        const int cg = (int)s.view[2 * c];
-        const int ce = (int)s.view[2 * c + 1];
-        const int take_eq = min(max(remaining - eq_before, 0), ce);
-        base += cg + take_eq;
+        const int ce = s.peer_counts[c][1];
+        base += s.peer_counts[c][0] + min(max(remaining - eq_before, 0), ce);
         eq_before += ce;
     }
-    int out_pos = base, eq_seen = eq_before;
-    for (int start = lo; start < hi; start += kThreads) {
-        const int i = start + tid;
-        const uint32_t key = i < hi ? key_at(i) : 0u;
-        const int g = (i < hi) && key > prefix;
-        const int e = (i < hi) && key == prefix;
-        int e_total, t_total;
-        const int e_rank = block_exclusive_scan(e, s.scan, e_total);
-        const int take = g || (e && eq_seen + e_rank < remaining);
-        const int pos = block_exclusive_scan(take, s.scan, t_total);
-        if (take && out_pos + pos < k) out[out_pos + pos] = i;
-        out_pos += t_total;
-        eq_seen += e_total;
+    const int take = gt + min(max(remaining - eq_before - eq_excl, 0), eq);
+    int tot_take;
+    int pos = base + block_exclusive_sum(take, s.wsum, tot_take);
+    int eq_seen = eq_before + eq_excl;
+    for (int j = 0; j < n_my; ++j) {
+        const uint32_t key = key_j(j);
+        bool keep = key > prefix;
+        if (key == prefix) {
+            keep = eq_seen < remaining;
+            ++eq_seen;
+        }
+        if (keep && pos < k) out[pos++] = mine + j;
     }
     if (crank == 0 && tid == 0) cnt_out[r] = k;
     ptx::cluster_sync();  // no CTA leaves while another may still read rank 0's counts
@@ -238,9 +212,10 @@ size_t topk_workspace_bytes(int, int, int, int) { return 0; }
 
 cudaError_t launch_topk(const float *logits, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap,
                         int m, int k, int32_t *idx_out, int32_t *cnt_out, void *, size_t, cudaStream_t stream) {
-    const int slice = (Ncap + kCtas - 1) / kCtas;
-    const int resident = slice <= kMaxResident ? 1 : 0;
-    const size_t smem = sizeof(TopkShared) + (resident ? (size_t)slice * sizeof(uint32_t) : 0);
+    const int per_cta = (Ncap + kCtas - 1) / kCtas;
+    const int run = (per_cta + kThreads - 1) / kThreads;
+    const int resident = run <= kMaxRun ? 1 : 0;
+    const size_t smem = sizeof(TopkShared) + (resident ? (size_t)run * kThreads * sizeof(uint32_t) : 0);
     cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -256,7 +231,7 @@ cudaError_t launch_topk(const float *logits, const int32_t *q_pos, const int32_t
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     count_launch();
-    e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, logits, q_pos, n_comp, T, Ncap, m, k, slice, resident, idx_out,
+    e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, logits, q_pos, n_comp, T, Ncap, m, k, run, resident, idx_out,
                            cnt_out);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
