@@ -34,6 +34,8 @@ struct TopkShared {
     alignas(16) uint32_t local[3][kBins];  // this CTA's histogram, one buffer per pass (read by every CTA)
     alignas(16) int counts[kCtas][2];      // rank 0's copy: (keys > K*, keys == K*) per CTA
     alignas(16) int peer_counts[kCtas][2];
+    alignas(16) uint32_t reduced[3][kBins / kCtas];  // this CTA's range of the cluster-wide histogram
+    int range_total[3][kCtas];                       // written by every CTA: its range's total
     int wsum[kWarps];
     uint32_t digit;
     int remaining;
@@ -118,16 +120,13 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
             if ((key & mask) == prefix) atomicAdd(&s.local[pass][(key >> shift) & dmask], 1u);
         }
         ptx::cluster_sync();  // every CTA's histogram of this pass is complete
-        // Thread t sums bins [d0, d0+4) over the 8 CTAs (one vector load of
-        // distributed shared memory each); threads take the bins from the
-        // largest digit down, so a block-wide scan finds the digit that holds
-        // the `remaining`-th largest matching key.
-        const int nb = (int)dmask + 1;
-        int c4[4] = {0, 0, 0, 0};
-        int tsum = 0, d0 = 0;
-        if (tid < nb / 4) {
-            d0 = nb - 4 * (tid + 1);
-            const uint32_t off = ptx::smem_u32(&s.local[pass][d0]);
+        // Reduce-scatter: CTA c sums bins [c * per, (c + 1) * per) over the 8
+        // CTAs (one vector load of distributed shared memory per CTA and 4
+        // bins) and publishes its range total to every CTA.
+        const int nb = (int)dmask + 1, per = nb / kCtas;
+        int part = 0;
+        if (tid < per / 4) {
+            const uint32_t off = ptx::smem_u32(&s.local[pass][crank * per + 4 * tid]);
             uint4 v[kCtas];
 #pragma unroll
             for (int c = 0; c < kCtas; ++c) v[c] = ld_cluster_v4(ptx::mapa(off, c));
@@ -139,24 +138,55 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
                 acc.z += v[c].z;
                 acc.w += v[c].w;
             }
-            c4[0] = (int)acc.w;  // digit d0 + 3
-            c4[1] = (int)acc.z;
-            c4[2] = (int)acc.y;
-            c4[3] = (int)acc.x;  // digit d0
-            tsum = c4[0] + c4[1] + c4[2] + c4[3];
+            reinterpret_cast<uint4 *>(s.reduced[pass])[tid] = acc;
+            part = (int)(acc.x + acc.y + acc.z + acc.w);
         }
-        int total;
-        const int excl = block_exclusive_sum(tsum, s.wsum, total);
-        if (tsum > 0 && excl < remaining && remaining <= excl + tsum) {
-            int cum = excl;
+        int range_tot;
+        block_exclusive_sum(part, s.wsum, range_tot);
+        if (tid < kCtas)
+            st_cluster_s32(ptx::mapa(ptx::smem_u32(&s.range_total[pass][crank]), tid), range_tot);
+        ptx::cluster_sync();  // every range total has arrived
+        // The range holding the `remaining`-th largest matching key (ranges of
+        // larger digits first); every CTA reads that range's bins and picks the
+        // same digit.
+        int owner = 0, above = 0;
+        for (int c = kCtas - 1; c >= 0; --c) {
+            const int t = s.range_total[pass][c];
+            if (above + t >= remaining) {
+                owner = c;
+                break;
+            }
+            above += t;
+        }
+        if (threadIdx.x < 32) {
+            const int lane = threadIdx.x;
+            const int bpl = per / 32;  // 8 or 4 bins per lane, lane 0 takes the largest
+            int cnt[8];
+            const uint32_t roff = ptx::mapa(ptx::smem_u32(&s.reduced[pass][per - bpl * (lane + 1)]), owner);
+            const uint4 hi4 = ld_cluster_v4(roff + (bpl == 8 ? 16u : 0u));
+            const uint4 lo4 = bpl == 8 ? ld_cluster_v4(roff) : make_uint4(0, 0, 0, 0);
+            cnt[0] = (int)hi4.w; cnt[1] = (int)hi4.z; cnt[2] = (int)hi4.y; cnt[3] = (int)hi4.x;
+            cnt[4] = (int)lo4.w; cnt[5] = (int)lo4.z; cnt[6] = (int)lo4.y; cnt[7] = (int)lo4.x;
+            int sum = 0;
+            for (int q = 0; q < bpl; ++q) sum += cnt[q];
+            int incl = sum;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (cum + c4[q] >= remaining) {
-                    s.digit = (uint32_t)(d0 + 3 - q);
-                    s.remaining = remaining - cum;
-                    break;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
+            }
+            const int need = remaining - above;
+            const int excl = incl - sum;
+            if (sum > 0 && excl < need && need <= incl) {
+                int cum = excl;
+                for (int q = 0; q < bpl; ++q) {
+                    if (cum + cnt[q] >= need) {
+                        s.digit = (uint32_t)(owner * per + per - 1 - (bpl * lane + q));
+                        s.remaining = need - cum;
+                        break;
+                    }
+                    cum += cnt[q];
                 }
-                cum += c4[q];
             }
         }
         __syncthreads();
