@@ -9,28 +9,37 @@
 //   z_j = scale * q_h . x_j,  o_h = sum_j e^{z_j-M} x_j / (e^{sink_h-M} + sum_j e^{z_j-M}),
 //   lse_h = M + ln(den),  M = max(sink_h, max_j z_j).
 //
-// Work unit = (query token, candidate split), run by a cluster of two CTAs;
-// CTA rank r owns latent dims [256 r, 256 r + 256):
-//   * Q[:, half] (128 heads x 256 BF16) lives in TMEM and is the A operand of
-//     QK; each CTA computes the partial scores of its half for a chunk of 64
-//     candidates (tcgen05.mma kind::f16, M=128 heads, N=64, K=256) and the two
-//     partials are exchanged through distributed shared memory, so both CTAs
-//     hold identical full scores and run an identical softmax.
-//   * P (BF16) is written back into the score columns of TMEM and is the A
-//     operand of PV: O[:, half] += P X[:, half] (M=128, N=256, K=64); O stays
-//     in TMEM (256 fp32 columns) across chunks.
-//   * Candidate bytes are gathered straight from the FP8/BF16 caches (TMA bulk
-//     copies, block-table strided) and dequantised in shared memory to BF16
-//     (code x block multiplier); there is no dequantised copy in HBM.
-// Warps: 0 gather producer, 1 MMA issuer (and TMEM owner), 2-5 dequantise,
-// 6-9 softmax / exchange / epilogue (thread = head). The running max is
-// rescaled lazily (only when it grows by more than 2^8), in the log2 domain.
-// With one split per query the CTA pair writes the BF16 output and LSE; with
-// several, each split writes a normalised BF16 partial and (max, sum), and a
-// combine kernel folds the splits and the sink. Every wait is bounded.
+// Work unit = (query token, candidate split, output half): two CTAs share a
+// (query, split); CTA r writes latent dims [256 r, 256 r + 256) of the output.
+// O (128 heads x 256 fp32) fills half of the tensor memory, so one CTA cannot
+// hold all 512 output dims; instead of exchanging partial scores between the
+// two halves (the SM-to-SM network moves only a few bytes per cycle), both
+// CTAs compute the full scores -- QK with K = 512 -- and run the softmax on
+// them, then each accumulates its own half of PV. Per CTA:
+//   * Q dims 0..383 live in TMEM (BF16 pairs) and dims 384..511 in shared
+//     memory; QK(j) = Q X_j^T (tcgen05.mma kind::f16, M = 128 heads, N = 64
+//     candidates, K = 512) lands in the TMEM score buffer. (A second score
+//     buffer would push Q operands into shared memory, whose bandwidth the
+//     QK reads already share with the dequantised stores.)
+//   * P (BF16, K-major rows in the 128-byte swizzle) is the A operand of
+//     PV: O += P X_j[:, half] (M = 128, N = 256, K = 64); O stays in TMEM.
+//   * Candidate records are copied straight from the FP8/BF16 caches into
+//     shared staging (16-byte cp.async, one chunk ahead, block-table
+//     resolved) and dequantised there to BF16 (code x block multiplier);
+//     there is no dequantised copy in HBM. X is kept as two halves, dims
+//     0..255 ("lo") and 256..511 ("hi"), each double-buffered: the half this
+//     CTA does not output is released as soon as QK has read it, its own half
+//     after PV.
+// Warps: 0 record-pointer producer, 1 MMA issuer (and TMEM owner), 2-9
+// load + dequantise, 10-13 softmax / epilogue (thread = head). The running max
+// is rescaled lazily (only when it grows by more than 2^8), in the log2
+// domain. With one split per query the CTAs write the BF16 output and LSE;
+// with several, each split writes a normalised BF16 partial and (max, sum),
+// and a combine kernel folds the splits and the sink. Every wait is bounded.
 #include <cuda.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -40,41 +49,64 @@ namespace csa {
 namespace {
 
 constexpr int kChunk = 64;                  // candidates per chunk
-constexpr int kHalf = 256;                  // latent dims per CTA
-constexpr int kSlot = 336;                  // staged bytes per candidate
-constexpr int kStages = 2;                  // staging ring depth (chunks)
-constexpr int kXBuf = 3;                    // dequantised chunk buffers
+constexpr int kHalf = 256;                  // output latent dims per CTA
+constexpr int kQTmemDims = 384;             // Q dims held in TMEM; the rest in shared memory
+constexpr int kPtrRing = 8;                 // chunks of resolved record pointers
 constexpr int kBatch = 4;                   // chunks whose indices the producer loads at once
-constexpr int kThreads = 320;               // 10 warps
+constexpr int kThreads = 448;               // 14 warps
 constexpr int kAtom = kChunk * 128;         // one 64-dim column block of X: 64 rows x 128 B
-constexpr int kXBytes = 4 * kAtom;          // 32 KB
+constexpr int kXHalfBytes = 4 * kAtom;      // 256 dims, 32 KB
+constexpr int kOwnBufs = 2;                 // buffers of the X half a CTA outputs (held until PV)
+constexpr int kOthBufs = 2;                 // buffers of the other half (held until QK)
+constexpr int kQAtom = kHeads * 128;        // one 64-dim column block of Q: 128 rows x 128 B
+constexpr int kConvWarps = 8;               // load + dequantise warps
+constexpr int kLoPieces = 4;                // per thread: codes 0..255 of a record in 16-byte pieces, 4 threads a row
+constexpr int kHiPieces = 5;                // per thread: codes 256..447 and the rope dims (3 + 2 pieces)
 constexpr uint64_t kWaitNs = 1000000000ull; // 1 s per wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazy = 8.f;                // rescale only when the max grows by > 2^8
 
-constexpr uint32_t kColQ = 0;    // 128 columns: Q half, BF16 pairs
-constexpr uint32_t kColO = 128;  // 256 columns: O half, fp32
-constexpr uint32_t kColS = 384;  // 2 x 64 columns: partial scores
+constexpr uint32_t kColQ = 0;    // 192 columns: Q dims 0..383, BF16 pairs
+constexpr uint32_t kColS = 192;  // 64 columns: scores
+constexpr uint32_t kColO = 256;  // 256 columns: O half, fp32
 constexpr uint32_t kTmemCols = 512;
 
-// recv[b] receives the peer's partial scores of a chunk ([16 float4][128
-// heads], fp32); p holds the chunk's P (128 heads x 64 candidates, BF16,
-// K-major rows of 128 B in the 128-byte swizzle), the A operand of PV.
+// Raw bytes of one half of a chunk's records. Thread t (row t / 4, quarter
+// c = t % 4) copies the half's 16-byte pieces c, c + 4, c + 8, ... into
+// piece[i][t] (consecutive threads touch consecutive words, in global and in
+// shared memory) and, for c = 0, the row's four block multipliers into
+// scale[row]. Lo: codes 0..255 (16 pieces a row); hi: codes 256..447 then
+// the 64 BF16 rope dims (20 pieces a row).
+template <int kPieces>
+struct HalfStage {
+    uint4 piece[kPieces][4 * kChunk];
+    float4 scale[kChunk];
+};
+
+// x_own / x_oth hold 64 candidates x 256 dims of a chunk (BF16, K-major rows
+// of 128 B in the 128-byte swizzle, 4 column blocks of 64 dims): the half of
+// the latent this CTA outputs, and the other half; qs holds Q dims 384..511
+// (2 column blocks); p holds P (128 heads x 64 candidates, BF16, swizzled
+// 128-byte rows), the A operand of PV.
 struct AttSmem {
-    alignas(1024) uint8_t x[kXBuf][kXBytes];    // dequantised candidates, 128-byte swizzle
-    alignas(1024) float4 recv[2][16 * kHeads];
+    alignas(1024) uint8_t x_own[kOwnBufs][kXHalfBytes];
+    alignas(1024) uint8_t x_oth[kOthBufs][kXHalfBytes];
+    alignas(1024) uint8_t qs[2 * kQAtom];
     alignas(1024) uint8_t p[kHeads * 128];
-    alignas(128) uint8_t stage[kStages][kChunk * kSlot];
-    uint64_t vmask[kStages], smask[kXBuf];
-    uint64_t stg_full[kStages], stg_empty[kStages];
-    uint64_t x_full[kXBuf], x_empty[kXBuf];
-    uint64_t s_full[2], s_free[2], p_full[2], rd_done[2];
-    uint64_t xchg_full[2], xchg_free[2];
+    alignas(16) HalfStage<kLoPieces> stage_lo;
+    alignas(16) HalfStage<kHiPieces> stage_hi;
+    const uint8_t *rec[kPtrRing][kChunk];       // record of each candidate (nullptr: skipped)
+    uint64_t vmask[kPtrRing];
+    uint64_t ptr_full[kPtrRing], ptr_empty[kPtrRing];
+    uint64_t own_full[kOwnBufs], own_empty[kOwnBufs], oth_full[kOthBufs], oth_empty[kOthBufs];
+    uint64_t s_full, s_free, p_full;
     uint64_t o_done[2], o_final, q_ready, mma_done;
     uint32_t tmem_base;
     int abort_flag;
 };
+
+static_assert(sizeof(AttSmem) + 1024 <= 232448, "shared memory plan exceeds the per-CTA limit");
 
 struct AttParams {
     const __nv_bfloat16 *q;
@@ -98,9 +130,9 @@ struct Unit {
 
 __device__ __forceinline__ Unit make_unit(const AttParams &P) {
     Unit u;
-    const int cluster = blockIdx.x >> 1;
-    u.r = cluster / P.n_split;
-    u.split = cluster % P.n_split;
+    const int pair = blockIdx.x >> 1;
+    u.r = pair / P.n_split;
+    u.split = pair % P.n_split;
     u.b = u.r / P.T;
     u.p = __ldg(P.q_pos + u.r);
     if (P.hca) {
@@ -138,57 +170,48 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w0, uint32_t w1, float s) {
     return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-// 16 E4M3 codes times a multiplier -> 16 BF16 values (two uint4).
-__device__ __forceinline__ void dequant16(uint4 c, float s, uint4 &lo, uint4 &hi) {
-    lo = dequant8(c.x, c.y, s);
-    hi = dequant8(c.z, c.w, s);
+// 16-byte chunk cc of row `row` of a swizzled block of 128-byte rows.
+__device__ __forceinline__ uint4 *sw128(uint8_t *block, int row, int cc) {
+    return reinterpret_cast<uint4 *>(block + row * 128 + ((cc ^ (row & 7)) << 4));
 }
 
-// One 64-dim block of a row in the 128-byte swizzle: 16-byte chunk cc of the
-// 128-byte row lands at position cc ^ (row & 7).
-__device__ __forceinline__ void store_atom_row(uint8_t *xa, int row, const uint4 (&v)[8]) {
-#pragma unroll
-    for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4 *>(xa + ((cc ^ (row & 7)) << 4)) = v[cc];
-}
-
-// Pipeline per chunk j (64 candidates), per CTA of the pair:
-//   producer:  gather raw bytes of chunk j            -> stage[j % 2]
-//   dequant:   stage -> X[j % 3] (BF16)               (after PV(j-3) freed it)
-//   MMA:       QK(j) -> S[j & 1] (after the softmax released S(j-2));
-//              PV(j) = P(j) X(j) -> O (after P(j) is ready); QK(j+2) is
-//              issued before PV(j), so scores run two chunks ahead
-//   softmax:   sends S(j+1) to the peer, combines S(j) with the peer's
-//              partial, releases S[j & 1] and (to the peer) recv[j & 1],
-//              writes P(j) into the P buffer once PV(j-1) is done
-//   PV(j) completion frees X[j % 3] and the P buffer.
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// Pipeline per chunk j (64 candidates), per CTA (b = j % 2; "oth" is the half
+// of X this CTA does not output, "own" the one it does):
+//   producer:  record pointers and validity mask of chunk j -> rec[j % 8]
+//   dequant:   oth(j) from the staging into x_oth[j % 2] (after QK(j-2)
+//              freed it), then copies oth(j+1) into the staging; the same for
+//              own(j) into x_own[j % 2] (after PV(j-2) freed it)
+//   MMA:       QK(j+1) -> S once the softmax has read S(j) (oth K-steps, then
+//              own), then PV(j) = P X(j)[:, own] -> O once P(j) is ready
+//   softmax:   reads S(j) and the mask, releases S, writes P(j) once PV(j-1)
+//              is done
+// QK(j) completion frees x_oth[j % 2]; PV(j) completion frees x_own[j % 2] and P.
+__global__ void __launch_bounds__(kThreads, 1)
 attention_tc_kernel(const AttParams P) {
     extern __shared__ uint8_t smem_raw[];
     AttSmem &s = *reinterpret_cast<AttSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = ptx::cluster_ctarank();
-    const uint32_t peer = rank ^ 1u;
+    const int rank = blockIdx.x & 1;  // output half: 0 = lo, 1 = hi
     volatile int *abort = &s.abort_flag;
     const Unit u = make_unit(P);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            ptx::mbar_init(&s.stg_full[i], 64);  // 32 copy-completion arrivals + 32 lane arrivals
-            ptx::mbar_init(&s.stg_empty[i], 4);
+        for (int i = 0; i < kPtrRing; ++i) {
+            ptx::mbar_init(&s.ptr_full[i], 32);  // every producer lane has written its pointers
+            ptx::mbar_init(&s.ptr_empty[i], kConvWarps + 4);  // every dequantise and softmax warp has read them
         }
-        for (int i = 0; i < kXBuf; ++i) {
-            ptx::mbar_init(&s.x_full[i], 4);
-            ptx::mbar_init(&s.x_empty[i], 1);
+        for (int i = 0; i < kOwnBufs; ++i) {
+            ptx::mbar_init(&s.own_full[i], kConvWarps);
+            ptx::mbar_init(&s.own_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(&s.s_full[i], 1);
-            ptx::mbar_init(&s.s_free[i], 4);
-            ptx::mbar_init(&s.p_full[i], 4);
-            ptx::mbar_init(&s.rd_done[i], 4);  // every softmax warp has read recv[i]
-            ptx::mbar_init(&s.xchg_full[i], 1);  // local expect_tx + the peer's st.async bytes
-            ptx::mbar_init(&s.xchg_free[i], 1);  // the peer has read its recv[i]
-            ptx::mbar_init(&s.o_done[i], 1);     // PV of a chunk of this parity is done
+        for (int i = 0; i < kOthBufs; ++i) {
+            ptx::mbar_init(&s.oth_full[i], kConvWarps);
+            ptx::mbar_init(&s.oth_empty[i], 1);
         }
+        ptx::mbar_init(&s.s_full, 1);
+        ptx::mbar_init(&s.s_free, 4);
+        ptx::mbar_init(&s.p_full, 4);
+        for (int i = 0; i < 2; ++i) ptx::mbar_init(&s.o_done[i], 1);  // PV of a chunk of this parity is done
         ptx::mbar_init(&s.o_final, 1);
         ptx::mbar_init(&s.q_ready, 4);
         ptx::mbar_init(&s.mma_done, 1);
@@ -198,7 +221,6 @@ attention_tc_kernel(const AttParams P) {
     if (warp == 1) ptx::tmem_alloc(&s.tmem_base, kTmemCols);
     ptx::tc_fence_before();
     __syncthreads();
-    ptx::cluster_sync();  // the peer's barriers exist before anyone signals them
     ptx::tc_fence_after();
     const uint32_t tmem = s.tmem_base;
 
@@ -209,15 +231,11 @@ attention_tc_kernel(const AttParams P) {
     auto wait = [&](uint64_t *bar, uint32_t parity) {
         return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort, kWaitNs)) != 0;
     };
-    auto wait_cluster = [&](uint64_t *bar, uint32_t parity) {
-        return __all_sync(0xffffffffu, ptx::mbar_wait_cluster(bar, parity, abort, kWaitNs)) != 0;
-    };
 
     if (warp == 0) {
-        // ------------------------------------------------------------ gather producer
+        // ------------------------------------------------------------ record-pointer producer
         // Candidate indices are loaded one batch (4 chunks) ahead; lane L holds
-        // candidates L + 32 q (q = 0..7) of the batch, i.e. candidates L and
-        // L + 32 of each of its 4 chunks.
+        // candidates L and L + 32 of each chunk of the batch.
         auto load_raw = [&](int g, int (&raw)[2 * kBatch]) {
 #pragma unroll
             for (int q = 0; q < 2 * kBatch; ++q) {
@@ -236,98 +254,111 @@ attention_tc_kernel(const AttParams P) {
             if (g + 1 < n_batches) load_raw(g + 1, nxt);
 #pragma unroll
             for (int cc = 0; cc < kBatch; ++cc) {
-                if (j >= u.n_chunks || !ok) break;
-                const int st = j % kStages;
-                if (!wait(&s.stg_empty[st], ((j / kStages) & 1) ^ 1)) { fail(); ok = false; break; }
+                if (j >= u.n_chunks) break;
+                const int pr = j % kPtrRing;
+                if (!wait(&s.ptr_empty[pr], ((j / kPtrRing) & 1) ^ 1)) { fail(); ok = false; break; }
                 bool valid[2];
-                const uint8_t *rec[2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int i = u.cb + j * kChunk + e * 32 + lane;
-                    rec[e] = nullptr;
+                    const uint8_t *rec = nullptr;
                     if (i < u.ce) {
                         if (i < u.n_sel) {
                             const int64_t ri = record_index(P.comp, u.b, cur[2 * cc + e]);
-                            if (ri >= 0) rec[e] = P.comp.base + ri * kRecBytes;
+                            if (ri >= 0) rec = P.comp.base + ri * kRecBytes;
                             else if (rank == 0) report_error(P.err, CSA_ERR_BAD_INDEX);
                         } else {
                             const int pos = u.j0 + (i - u.n_sel);
-                            rec[e] = P.ring + ((int64_t)u.b * P.R + pos % P.R) * kRecBytes;
+                            rec = P.ring + ((int64_t)u.b * P.R + pos % P.R) * kRecBytes;
                         }
                     }
-                    valid[e] = rec[e] != nullptr;
+                    valid[e] = rec != nullptr;
+                    s.rec[pr][e * 32 + lane] = rec;
                 }
-                // each lane copies its two candidates' bytes in 16-byte pieces:
-                // rank 0 bytes [0,256) + [576,592), rank 1 bytes [256,592)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    if (!valid[e]) continue;
-                    uint8_t *dst = s.stage[st] + (e * 32 + lane) * kSlot;
-                    if (rank == 0) {
-#pragma unroll
-                        for (int pc = 0; pc < 16; ++pc) ptx::cp_async_16(dst + pc * 16, rec[e] + pc * 16);
-                        ptx::cp_async_16(dst + 256, rec[e] + kScaleOffset);
-                    } else {
-#pragma unroll
-                        for (int pc = 0; pc < 21; ++pc) ptx::cp_async_16(dst + pc * 16, rec[e] + 256 + pc * 16);
-                    }
-                }
-                ptx::cp_async_arrive_noinc(&s.stg_full[st]);
                 const uint32_t m0 = __ballot_sync(0xffffffffu, valid[0]);
                 const uint32_t m1 = __ballot_sync(0xffffffffu, valid[1]);
-                if (lane == 0) s.vmask[st] = (uint64_t)m0 | ((uint64_t)m1 << 32);
+                if (lane == 0) s.vmask[pr] = (uint64_t)m0 | ((uint64_t)m1 << 32);
                 __syncwarp();
-                ptx::mbar_arrive(&s.stg_full[st]);
+                ptx::mbar_arrive(&s.ptr_full[pr]);
                 ++j;
             }
         }
-        // drain: every issued copy has landed before the CTA may exit
-        for (int q = (j > kStages ? j - kStages : 0); q < j; ++q) wait(&s.stg_full[q % kStages], (q / kStages) & 1);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         constexpr uint32_t kIdescQK = ptx::idesc_f32acc(1, 1, 128, kChunk);
         constexpr uint32_t kIdescPV = ptx::idesc_f32acc(1, 1, 128, kHalf, 1);
         bool ok = u.n_chunks == 0 || wait(&s.q_ready, 0);
         if (!ok) fail();
+        // The 16 K-steps of one X half (dims 256 HF + 16 kl + ...): Q from TMEM
+        // below dim 256, from shared memory above. The half is a template
+        // argument and each step's descriptor is the base descriptor plus a
+        // constant (the start-address field counts 16-byte units), so the
+        // issue loop is little more than the MMA instructions themselves.
+        auto qk_half = [&](auto hf_tag, const uint8_t *xbuf, bool first) {
+            constexpr int HF = decltype(hf_tag)::value;
+            constexpr int kTs = HF == 0 ? 16 : (kQTmemDims / 16 > 16 ? kQTmemDims / 16 - 16 : 0);  // Q in TMEM
+            const uint64_t xd = ptx::desc_kmajor_sw128(ptx::smem_u32(xbuf));
+            const uint64_t qd = ptx::desc_kmajor_sw128(ptx::smem_u32(s.qs));
+#pragma unroll
+            for (int kl = 0; kl < kTs; ++kl)
+                ptx::mma_f16_ts(tmem + kColS, tmem + kColQ + (16 * HF + kl) * 8,
+                                xd + (uint64_t)(((kl >> 2) * kAtom + (kl & 3) * 32) >> 4), kIdescQK,
+                                (first && kl == 0) ? 0u : 1u);
+#pragma unroll
+            for (int kl = kTs; kl < 16; ++kl) {
+                const int kq = 16 * HF + kl - kQTmemDims / 16;
+                ptx::mma_f16(tmem + kColS, qd + (uint64_t)(((kq >> 2) * kQAtom + (kq & 3) * 32) >> 4),
+                             xd + (uint64_t)(((kl >> 2) * kAtom + (kl & 3) * 32) >> 4), kIdescQK,
+                             (first && kTs == 0 && kl == 0) ? 0u : 1u);
+            }
+        };
+        using Lo = std::integral_constant<int, 0>;
+        using Hi = std::integral_constant<int, 1>;
+        // QK(jq) -> S once the softmax has read S(jq-1): the half this CTA does
+        // not output first (it is converted first), then its own half.
         auto issue_qk = [&](int jq) -> bool {
-            const int xb = jq % kXBuf, sb = jq & 1;
-            if (!wait(&s.x_full[xb], (jq / kXBuf) & 1)) return false;
-            if (jq >= 2 && !wait(&s.s_free[sb], ((jq - 2) >> 1) & 1)) return false;
+            const int ob = jq % kOthBufs, wb = jq % kOwnBufs;
+            if (!wait(&s.oth_full[ob], (jq / kOthBufs) & 1)) return false;
+            if (jq >= 1 && !wait(&s.s_free, (jq - 1) & 1)) return false;
             ptx::tc_fence_after();
             if (lane == 0) {
-                const uint32_t xa = ptx::smem_u32(s.x[xb]);
-#pragma unroll
-                for (int kk = 0; kk < kHalf / 16; ++kk)
-                    ptx::mma_f16_ts(tmem + kColS + sb * kChunk, tmem + kColQ + kk * 8,
-                                    ptx::desc_kmajor_sw128(xa + (kk >> 2) * kAtom + (kk & 3) * 32), kIdescQK,
-                                    kk > 0 ? 1u : 0u);
-                ptx::mma_commit(&s.s_full[sb]);
+                if (rank == 0) qk_half(Hi{}, s.x_oth[ob], true);
+                else qk_half(Lo{}, s.x_oth[ob], true);
+                ptx::mma_commit(&s.oth_empty[ob]);
+            }
+            __syncwarp();
+            if (!wait(&s.own_full[wb], (jq / kOwnBufs) & 1)) return false;
+            ptx::tc_fence_after();
+            if (lane == 0) {
+                if (rank == 0) qk_half(Lo{}, s.x_own[wb], false);
+                else qk_half(Hi{}, s.x_own[wb], false);
+                ptx::mma_commit(&s.s_full);
             }
             __syncwarp();
             return true;
         };
         auto issue_pv = [&](int jp) -> bool {
-            const int xb = jp % kXBuf, pb = jp & 1;
-            if (!wait(&s.p_full[pb], (jp >> 1) & 1)) return false;
+            const int wb = jp % kOwnBufs;
+            if (!wait(&s.p_full, jp & 1)) return false;
             ptx::tc_fence_after();
             if (lane == 0) {
-                const uint32_t xa = ptx::smem_u32(s.x[xb]);
+                const uint32_t xa = ptx::smem_u32(s.x_own[wb]);
                 const uint32_t pa = ptx::smem_u32(s.p);
+                const uint64_t ad = ptx::desc_kmajor_sw128(pa);
+                const uint64_t bd = ptx::desc_mnmajor_sw128(xa, kAtom, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kChunk / 16; ++kk)
-                    ptx::mma_f16(tmem + kColO, ptx::desc_kmajor_sw128(pa + kk * 32),
-                                 ptx::desc_mnmajor_sw128(xa + kk * 2048, kAtom, 1024), kIdescPV,
+                    ptx::mma_f16(tmem + kColO, ad + (uint64_t)(kk * 32 >> 4), bd + (uint64_t)(kk * 2048 >> 4), kIdescPV,
                                  (jp > 0 || kk > 0) ? 1u : 0u);
-                ptx::mma_commit(&s.x_empty[xb]);
-                ptx::mma_commit(&s.o_done[pb]);
+                ptx::mma_commit(&s.own_empty[wb]);
+                ptx::mma_commit(&s.o_done[jp & 1]);
             }
             __syncwarp();
             return true;
         };
         if (ok && u.n_chunks > 0 && !issue_qk(0)) { fail(); ok = false; }
-        if (ok && u.n_chunks > 1 && !issue_qk(1)) { fail(); ok = false; }
         for (int j = 0; j < u.n_chunks && ok; ++j) {
-            if (j + 2 < u.n_chunks && !issue_qk(j + 2)) { fail(); ok = false; break; }
+            if (j + 1 < u.n_chunks && !issue_qk(j + 1)) { fail(); ok = false; break; }
             if (!issue_pv(j)) { fail(); ok = false; break; }
         }
         if (lane == 0) {
@@ -336,155 +367,172 @@ attention_tc_kernel(const AttParams P) {
         }
         __syncwarp();
         wait(&s.mma_done, 0);
-    } else if (warp < 6) {
-        // ------------------------------------------------------------ dequantise
-        const int ct = threadIdx.x - 64;  // 0..127
-        const int ci = ct >> 1;           // candidate row of the chunk
-        const int half = ct & 1;          // local dims [128 half, 128 half + 128)
-        bool ok = true;
-        for (int j = 0; j < u.n_chunks && ok; ++j) {
-            const int st = j % kStages, xb = j % kXBuf;
-            if (!wait(&s.stg_full[st], (j / kStages) & 1)) { fail(); ok = false; break; }
-            if (!wait(&s.x_empty[xb], ((j / kXBuf) & 1) ^ 1)) { fail(); ok = false; break; }
-            const uint64_t mask = s.vmask[st];
-            const bool valid = (mask >> ci) & 1ull;
-            const uint8_t *slot = s.stage[st] + ci * kSlot;
-            uint8_t *xrow = s.x[xb] + ci * 128;
-            // this thread's two 64-dim blocks of the row: local dims [128 half, 128 half + 128)
-            // rank 0: latent dims 128 half + ..., one multiplier (block `half`)
-            // rank 1: half 0 -> latent 256..383 (block 2); half 1 -> latent 384..447
-            //         (block 3) then the 64 rope dims (BF16, copied)
-            uint4 v[2][8];
-            if (valid) {
-                const uint4 *codes = reinterpret_cast<const uint4 *>(slot + 128 * half);
-                if (rank == 0 || half == 0) {
-                    const float sc = *reinterpret_cast<const float *>(slot + (rank == 0 ? 256 + 4 * half : 320 + 8));
-                    uint4 cv[8];
+    } else if (warp < 2 + kConvWarps) {
+        // ------------------------------------------------------------ load + dequantise
+        const int ct = threadIdx.x - 64;  // 0..255
+        const int row = ct >> 2, hq = ct & 3;
+        const int own_hf = rank, oth_hf = rank ^ 1;
+        auto fetch_ptr = [&](int jj, const uint8_t *&rec) -> bool {
+            const int pr = jj % kPtrRing;
+            if (!wait(&s.ptr_full[pr], (jj / kPtrRing) & 1)) return false;
+            rec = s.rec[pr][row];
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&s.ptr_empty[pr]);
+            return true;
+        };
+        // copies this thread's pieces of half hf of record `rec` into the half's staging
+        auto load_half = [&](int hf, const uint8_t *rec) {
+            if (!rec) return;
+            if (hf == 0) {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) cv[q] = codes[q];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) dequant16(cv[q], sc, v[q >> 2][(q & 3) * 2], v[q >> 2][(q & 3) * 2 + 1]);
-                } else {
-                    const float sc = *reinterpret_cast<const float *>(slot + 320 + 12);
-                    uint4 cv[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) cv[q] = codes[q];
-                    const uint4 *rope = reinterpret_cast<const uint4 *>(slot + 192);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) v[1][q] = rope[q];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) dequant16(cv[q], sc, v[0][2 * q], v[0][2 * q + 1]);
-                }
+                for (int i = 0; i < kLoPieces; ++i) ptx::cp_async_16(&s.stage_lo.piece[i][ct], rec + 16 * (hq + 4 * i));
+                if (hq == 0) ptx::cp_async_16(&s.stage_lo.scale[row], rec + kScaleOffset);
             } else {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) v[0][q] = v[1][q] = make_uint4(0, 0, 0, 0);
+                for (int i = 0; i < kHiPieces; ++i)
+                    ptx::cp_async_16(&s.stage_hi.piece[i][ct], rec + 256 + 16 * (hq + 4 * i));
+                if (hq == 0) ptx::cp_async_16(&s.stage_hi.scale[row], rec + kScaleOffset);
             }
-            store_atom_row(xrow + (2 * half) * kAtom, ci, v[0]);
-            store_atom_row(xrow + (2 * half + 1) * kAtom, ci, v[1]);
-            ptx::fence_proxy_async_smem();  // generic-proxy stores -> MMA (async proxy) reads
-            if (ct == 0) s.smask[xb] = mask;
-            __syncwarp();
-            if (lane == 0) {
-                ptx::mbar_arrive(&s.stg_empty[st]);
-                ptx::mbar_arrive(&s.x_full[xb]);
+        };
+        // Piece hq + 4 i of a half: code pieces hold 16 dims starting at
+        // 16 (hq + 4 i) within the half -> column block i, 16-byte chunks 2 hq
+        // and 2 hq + 1, block multiplier i / 2; the hi half's pieces 12..19
+        // (i = 3, 4) are the rope dims 448 + 8 (piece - 12)... -> column block
+        // 3, chunk piece - 12 (copied as they are). The loops stay rolled: the
+        // hot code of all four warp roles shares each scheduler's instruction
+        // cache.
+        auto convert_codes = [&](uint8_t *xs, const uint4 *pieces, int n, float m_lo, float m_hi, bool valid) {
+            const uint4 zero = make_uint4(0, 0, 0, 0);
+#pragma unroll 1
+            for (int i = 0; i < n; ++i) {
+                uint4 lo = zero, hi = zero;
+                if (valid) {
+                    const uint4 c = pieces[i * 4 * kChunk + ct];
+                    const float mult = (i >> 1) ? m_hi : m_lo;
+                    lo = dequant8(c.x, c.y, mult);
+                    hi = dequant8(c.z, c.w, mult);
+                }
+                uint8_t *atom = xs + i * kAtom;
+                *sw128(atom, row, 2 * hq) = lo;
+                *sw128(atom, row, 2 * hq + 1) = hi;
             }
+        };
+        auto convert_half = [&](int hf, uint8_t *xs, bool valid) {
+            if (hf == 0) {
+                const float4 sc = valid ? s.stage_lo.scale[row] : make_float4(0.f, 0.f, 0.f, 0.f);
+                convert_codes(xs, &s.stage_lo.piece[0][0], kLoPieces, sc.x, sc.y, valid);
+            } else {
+                const float4 sc = valid ? s.stage_hi.scale[row] : make_float4(0.f, 0.f, 0.f, 0.f);
+                convert_codes(xs, &s.stage_hi.piece[0][0], 3, sc.z, sc.w, valid);
+#pragma unroll
+                for (int i = 3; i < kHiPieces; ++i)
+                    *sw128(xs + 3 * kAtom, row, hq + 4 * (i - 3)) =
+                        valid ? s.stage_hi.piece[i][ct] : make_uint4(0, 0, 0, 0);
+            }
+        };
+        // cp.async groups, oldest first: oth(0), own(0), then per chunk j
+        // oth(j+1) and own(j+1) (empty past the last chunk), so "at most one
+        // pending" before each conversion means the half about to be converted
+        // has landed.
+        bool ok = true;
+        const uint8_t *rec_nxt = nullptr;
+        if (u.n_chunks > 0) {
+            if (!fetch_ptr(0, rec_nxt)) { fail(); ok = false; }
+            if (ok) load_half(oth_hf, rec_nxt);
+            ptx::cp_async_commit();
+            if (ok) load_half(own_hf, rec_nxt);
+            ptx::cp_async_commit();
         }
+        for (int j = 0; j < u.n_chunks && ok; ++j) {
+            const int ob = j % kOthBufs, wb = j % kOwnBufs;
+            const uint8_t *rec_cur = rec_nxt;
+            // ---- other half of chunk j
+            ptx::cp_async_wait<1>();
+            __syncwarp();  // the row's multipliers (copied by its first thread) are visible to all four
+            if (!wait(&s.oth_empty[ob], ((j / kOthBufs) & 1) ^ 1)) { fail(); ok = false; break; }
+            convert_half(oth_hf, s.x_oth[ob], rec_cur != nullptr);
+            ptx::fence_proxy_async_smem();  // generic-proxy stores -> MMA (async proxy) reads
+            __syncwarp();                   // (and the row's threads are done with the staging)
+            if (lane == 0) ptx::mbar_arrive(&s.oth_full[ob]);
+            if (j + 1 < u.n_chunks) {
+                if (!fetch_ptr(j + 1, rec_nxt)) { fail(); ok = false; break; }
+                load_half(oth_hf, rec_nxt);
+            }
+            ptx::cp_async_commit();
+            // ---- own half of chunk j
+            ptx::cp_async_wait<1>();
+            __syncwarp();
+            if (!wait(&s.own_empty[wb], ((j / kOwnBufs) & 1) ^ 1)) { fail(); ok = false; break; }
+            convert_half(own_hf, s.x_own[wb], rec_cur != nullptr);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&s.own_full[wb]);
+            if (j + 1 < u.n_chunks) load_half(own_hf, rec_nxt);
+            ptx::cp_async_commit();
+        }
+        ptx::cp_async_wait<0>();  // no copy lands after this warp has moved on
     } else {
-        // ------------------------------------------------------------ softmax / exchange / epilogue
+        // ------------------------------------------------------------ softmax / epilogue
         const int quarter = warp & 3;
         const int h = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const int r = u.r;
         bool ok = true;
-        // Q half -> TMEM (BF16 pairs, lane = head)
+        // Q: dims 256..511 -> shared memory (cp.async), dims 0..255 -> TMEM
+        // (BF16 pairs, lane = head), 128 dims per round trip
         if (u.n_chunks > 0) {
-            const uint4 *qg = reinterpret_cast<const uint4 *>(P.q + ((size_t)r * kHeads + h) * kDim + rank * kHalf);
+            const uint4 *qg = reinterpret_cast<const uint4 *>(P.q + ((size_t)r * kHeads + h) * kDim);
 #pragma unroll
-            for (int piece = 0; piece < 4; ++piece) {
-                uint32_t regs[32];
+            for (int c = 0; c < (kDim - kQTmemDims) / 8; ++c)
+                ptx::cp_async_16(sw128(s.qs + (c >> 3) * kQAtom, h, c & 7), qg + kQTmemDims / 8 + c);
+            ptx::cp_async_commit();
+#pragma unroll 1
+            for (int pp = 0; pp < kQTmemDims / 128; ++pp) {
+                uint4 w[16];
 #pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                    const uint4 w4 = __ldg(qg + piece * 8 + v);
-                    regs[4 * v] = w4.x;
-                    regs[4 * v + 1] = w4.y;
-                    regs[4 * v + 2] = w4.z;
-                    regs[4 * v + 3] = w4.w;
+                for (int v = 0; v < 16; ++v) w[v] = __ldg(qg + pp * 16 + v);
+#pragma unroll
+                for (int hp = 0; hp < 2; ++hp) {
+                    uint32_t regs[32];
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        regs[4 * v] = w[8 * hp + v].x;
+                        regs[4 * v + 1] = w[8 * hp + v].y;
+                        regs[4 * v + 2] = w[8 * hp + v].z;
+                        regs[4 * v + 3] = w[8 * hp + v].w;
+                    }
+                    ptx::tmem_st32(lane_base + kColQ + (2 * pp + hp) * 32, regs);
                 }
-                ptx::tmem_st32(lane_base + kColQ + piece * 32, regs);
             }
+            ptx::cp_async_wait<0>();
             ptx::tmem_st_wait();
+            ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&s.q_ready);
         }
-        const uint32_t recv_peer[2] = {ptx::mapa(ptx::smem_u32(s.recv[0]), peer),
-                                       ptx::mapa(ptx::smem_u32(s.recv[1]), peer)};
-        const uint32_t full_peer[2] = {ptx::mapa(ptx::smem_u32(&s.xchg_full[0]), peer),
-                                       ptx::mapa(ptx::smem_u32(&s.xchg_full[1]), peer)};
-        const uint32_t free_peer[2] = {ptx::mapa(ptx::smem_u32(&s.xchg_free[0]), peer),
-                                       ptx::mapa(ptx::smem_u32(&s.xchg_free[1]), peer)};
         float m = -INFINITY, l = 0.f;  // running max and sum, log2 domain, sink not included
-        // Sends this CTA's partial scores of chunk jj into the peer's recv
-        // (st.async, completing bytes on the peer's xchg_full barrier) once the
-        // peer has read chunk jj-2 out of that buffer, and arms the local
-        // receive barrier of chunk jj.
-        auto send = [&](int jj) -> bool {
-            const int b2 = jj & 1;
-            if (!wait(&s.s_full[b2], (jj >> 1) & 1)) return false;
+        for (int j = 0; j < u.n_chunks && ok; ++j) {
+            const int pr = j % kPtrRing;
+            if (!wait(&s.ptr_full[pr], (j / kPtrRing) & 1)) { fail(); ok = false; break; }
+            const uint64_t mask = s.vmask[pr];
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&s.ptr_empty[pr]);
+            if (!wait(&s.s_full, j & 1)) { fail(); ok = false; break; }
             ptx::tc_fence_after();
             uint32_t sa[32], sb[32];
-            ptx::tmem_ld32(lane_base + kColS + b2 * kChunk, sa);
-            ptx::tmem_ld32(lane_base + kColS + b2 * kChunk + 32, sb);
-            ptx::tmem_ld_wait();
-            if (threadIdx.x == 192) ptx::mbar_arrive_expect_tx(&s.xchg_full[b2], 16 * kHeads * 16);
-            if (jj >= 2 && !wait_cluster(&s.xchg_free[b2], ((jj - 2) >> 1) & 1)) return false;
-#pragma unroll
-            for (int cq = 0; cq < 8; ++cq) {
-                ptx::st_async_v4(recv_peer[b2] + (uint32_t)((cq * kHeads + h) * 16),
-                                 make_float4(__uint_as_float(sa[4 * cq]), __uint_as_float(sa[4 * cq + 1]),
-                                             __uint_as_float(sa[4 * cq + 2]), __uint_as_float(sa[4 * cq + 3])),
-                                 full_peer[b2]);
-                ptx::st_async_v4(recv_peer[b2] + (uint32_t)(((8 + cq) * kHeads + h) * 16),
-                                 make_float4(__uint_as_float(sb[4 * cq]), __uint_as_float(sb[4 * cq + 1]),
-                                             __uint_as_float(sb[4 * cq + 2]), __uint_as_float(sb[4 * cq + 3])),
-                                 full_peer[b2]);
-            }
-            return true;
-        };
-        if (u.n_chunks > 0 && !send(0)) { fail(); ok = false; }
-        for (int j = 0; j < u.n_chunks && ok; ++j) {
-            const int jb = j & 1, xb = j % kXBuf;
-            if (j + 1 < u.n_chunks && !send(j + 1)) { fail(); ok = false; break; }
-            if (!wait_cluster(&s.xchg_full[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
-            // own partial of chunk j from TMEM, then release the score buffer
-            uint32_t sa[32], sb[32];
-            ptx::tmem_ld32(lane_base + kColS + jb * kChunk, sa);
-            ptx::tmem_ld32(lane_base + kColS + jb * kChunk + 32, sb);
+            ptx::tmem_ld32(lane_base + kColS, sa);
+            ptx::tmem_ld32(lane_base + kColS + 32, sb);
             ptx::tmem_ld_wait();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&s.s_free[jb]);
+            if (lane == 0) ptx::mbar_arrive(&s.s_free);
             float z[kChunk];
-#pragma unroll
-            for (int cq = 0; cq < 16; ++cq) {
-                const float4 pv = s.recv[jb][cq * kHeads + h];
-                const uint32_t *own = cq < 8 ? &sa[4 * cq] : &sb[4 * (cq - 8)];
-                z[4 * cq + 0] = __uint_as_float(own[0]) + pv.x;
-                z[4 * cq + 1] = __uint_as_float(own[1]) + pv.y;
-                z[4 * cq + 2] = __uint_as_float(own[2]) + pv.z;
-                z[4 * cq + 3] = __uint_as_float(own[3]) + pv.w;
-            }
-            // once every softmax thread has read recv[jb], the peer may refill it
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&s.rd_done[jb]);
-            if (!wait(&s.rd_done[jb], (j >> 1) & 1)) { fail(); ok = false; break; }
-            if (threadIdx.x == 192) ptx::mbar_arrive_remote(free_peer[jb]);
-            if (!wait(&s.x_full[xb], (j / kXBuf) & 1)) { fail(); ok = false; break; }
-            const uint64_t mask = s.smask[xb];
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int c = 0; c < kChunk; ++c) {
-                z[c] = ((mask >> c) & 1ull) ? z[c] * P.scale_log2 : -INFINITY;
+                const float sv = __uint_as_float(c < 32 ? sa[c] : sb[c - 32]);
+                z[c] = ((mask >> c) & 1ull) ? sv * P.scale_log2 : -INFINITY;
                 mx4[c & 3] = fmaxf(mx4[c & 3], z[c]);
             }
             const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
@@ -496,8 +544,9 @@ attention_tc_kernel(const AttParams P) {
                 const float alpha = need ? ptx::ex2_approx(m - mx) : 1.f;  // 0 when m = -inf
                 if (j > 0) {
                     // O holds PV of chunks < j: wait for the last one, then rescale in place.
-                    // (PV(j-3) is done -- it freed X for chunk j -- so this barrier is at
-                    // most one phase behind and the parity test is unambiguous.)
+                    // (This thread saw PV(j-2) done before writing P(j-1), and PV(j-3)
+                    // completed before it, so the barrier is at most one phase
+                    // behind and the parity test is unambiguous.)
                     if (!wait(&s.o_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) { fail(); ok = false; break; }
                     ptx::tc_fence_after();
 #pragma unroll 1
@@ -515,14 +564,13 @@ attention_tc_kernel(const AttParams P) {
                 l *= alpha;
                 if (need) m = mx;
             }
-            // P(j) = 2^(z - m) as BF16 rows (K-major, 128-byte swizzle), once PV(j-1)
-            // has finished reading the previous P
+            // P(j) = 2^(z - m) as BF16 (the head's swizzled 128-byte row), once
+            // PV(j-1) has finished reading the previous P
             if (j > 0 && !wait(&s.o_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) { fail(); ok = false; break; }
             const float mref = (m == -INFINITY) ? 0.f : m;  // every z is -inf while m is
             float ps4[4] = {0.f, 0.f, 0.f, 0.f};
-            uint8_t *prow = s.p + h * 128;
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
+            for (int c8 = 0; c8 < kChunk / 8; ++c8) {
                 uint32_t w[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -531,12 +579,12 @@ attention_tc_kernel(const AttParams P) {
                     ps4[i] += p0 + p1;
                     w[i] = bf16x2_bits(p0, p1);
                 }
-                *reinterpret_cast<uint4 *>(prow + ((c8 ^ (h & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *sw128(s.p, h, c8) = make_uint4(w[0], w[1], w[2], w[3]);
             }
             l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
             ptx::fence_proxy_async_smem();  // P stores -> PV (async proxy) reads
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&s.p_full[jb]);
+            if (lane == 0) ptx::mbar_arrive(&s.p_full);
         }
         // ---------------- epilogue: O half (and LSE) out
         if (ok && u.n_chunks > 0) {
@@ -589,7 +637,6 @@ attention_tc_kernel(const AttParams P) {
 
     ptx::tc_fence_before();
     __syncthreads();
-    ptx::cluster_sync();  // no remote access to this CTA's shared memory after this point
     ptx::tc_fence_after();
     if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
 }

@@ -319,6 +319,15 @@ __device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gsrc) {
                  : "memory");
 }
 
+// Closes this thread's current group of cp.async copies.
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Waits until at most N of this thread's committed cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Arrive on `bar` once every cp.async this thread issued so far has landed
 // (the barrier's expected count includes this arrival).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
@@ -346,6 +355,29 @@ __device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta
 // Named barrier over `count` threads (id > 0; id 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+
+// Bulk copy from this CTA's shared memory into another CTA's shared memory of
+// the cluster (dst and bar are shared::cluster addresses, e.g. from mapa),
+// completing `bytes` transaction bytes on the remote barrier. Its completion
+// (and the end of its reads of `src`) is observable only through that barrier.
+__device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst_cluster, const void *src, uint32_t bytes,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster),
+        "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+        : "memory");
+}
+
+// 16-byte read-only global load that does not allocate in L1.
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
 }
 
 }  // namespace ptx
