@@ -9,14 +9,16 @@
 // c >= n_vis(b,t) get -inf ("DSV4 Audit", section A3, item 1).
 //
 // Design (one persistent CTA per SM, 10 warps):
-//   warp 0   TMA producer: 128-key x 128-byte FP8 tiles (128-byte swizzle) into
-//            an 8-stage shared-memory ring; per sequence, the T*64 query rows
-//            (FP8) and the head weights w*sq into one of two query slots.
-//   warp 1   MMA issuer: tcgen05.mma kind::f8f6f4, M = 128 keys, N = 64*T
-//            query-head rows, K = 128 (4 x K32), fp32 accumulator in TMEM,
-//            two accumulator buffers so the epilogue overlaps the next tile.
+//   warp 0   TMA producer: 256-key (T <= 2; else 128-key) x 128-byte FP8
+//            tiles (128-byte swizzle) into a 6-stage (8-stage) shared-memory
+//            ring; per sequence, the T*64 query rows (FP8) and the head
+//            weights w*sq into one of two query slots.
+//   warp 1   MMA issuer: tcgen05.mma kind::f8f6f4, M = 128 keys per MMA (two
+//            halves of a 256-key tile), N = 64*T query-head rows, K = 128
+//            (4 x K32), fp32 accumulators in TMEM, up to four tiles deep so the
+//            epilogue overlaps the next tiles.
 //   warps 2-9 epilogue, two groups of 4 taking alternate tiles: thread i owns
-//            TMEM lane i = key c0+i; it reads the 64*T head dot products,
+//            TMEM lane i = key c0+i of each 128-key half; it reads the 64*T head dot products,
 //            applies ReLU and the head weights, scales by the key's scale and
 //            writes the row of logits (coalesced). Up to four accumulator
 //            buffers let the MMA run ahead of both groups.
@@ -33,19 +35,33 @@ namespace csa {
 
 namespace {
 
-constexpr int kTileKeys = 128;
-constexpr int kStages = 8;
-constexpr int kTileBytes = kTileKeys * kIdxDim;  // 16 KB
 constexpr int kThreads = 320;  // producer, MMA, two 4-warp epilogue groups
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
+// Tile shape per tokens-per-sequence T: a tile is kHalves blocks of 128 keys
+// (one M = 128 MMA each); 256-key tiles halve the fixed per-tile costs
+// (barrier waits, commits, bookkeeping) where TMEM still holds four
+// accumulators (T <= 2).
+template <int T>
+struct IdxCfg {
+    static constexpr int kHalves = T <= 2 ? 2 : 1;
+    static constexpr int kTileKeys = 128 * kHalves;
+    static constexpr int kStages = kHalves == 2 ? 6 : 8;
+    static constexpr int kTileBytes = kTileKeys * kIdxDim;  // 32 KB or 16 KB
+    static constexpr int N = T * kIdxHeads;                 // accumulator columns per 128 keys
+    static constexpr int kAccCols = kHalves * N;            // per tile
+    static constexpr int kAcc = (4 * kAccCols <= 512) ? 4 : 2;
+    static constexpr uint32_t kTmemCols = (kAcc * kAccCols <= 128) ? 128 : (kAcc * kAccCols <= 256 ? 256 : 512);
+};
+
 template <int T>
 struct IdxSmem {
+    using C = IdxCfg<T>;
     static constexpr int kQBytes = T * kIdxHeads * kIdxDim;  // T * 8 KB
-    alignas(1024) uint8_t keys[kStages][kTileBytes];
+    alignas(1024) uint8_t keys[C::kStages][C::kTileBytes];
     alignas(1024) uint8_t q[2][kQBytes];
     float ws[2][T * kIdxHeads];  // w * sq per query slot
-    uint64_t full[kStages], empty[kStages];
+    uint64_t full[C::kStages], empty[C::kStages];
     uint64_t acc_full[4], acc_empty[4];
     uint64_t q_full[2], q_empty[2];
     uint64_t mma_done;
@@ -72,10 +88,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                   const float *__restrict__ q_scale, const float *__restrict__ w_idx,
                   const float *__restrict__ k_scale, const int32_t *__restrict__ q_pos,
                   const int32_t *__restrict__ n_comp, int B, int Ncap, int m, float *__restrict__ logits, int *err) {
-    constexpr int N = T * kIdxHeads;
-    constexpr int kAcc = (4 * N <= 512) ? 4 : 2;  // TMEM accumulator buffers
-    constexpr uint32_t kTmemCols = (kAcc * N <= 128) ? 128 : (kAcc * N <= 256 ? 256 : 512);
-    constexpr uint32_t kIdesc = ptx::idesc_f32acc(0, 0, kTileKeys, N);
+    using C = IdxCfg<T>;
+    constexpr int N = C::N;
+    constexpr int kHalves = C::kHalves, kTileKeys = C::kTileKeys, kStages = C::kStages, kTileBytes = C::kTileBytes;
+    constexpr int kAcc = C::kAcc, kAccCols = C::kAccCols;
+    constexpr uint32_t kTmemCols = C::kTmemCols;
+    constexpr uint32_t kIdesc = ptx::idesc_f32acc(0, 0, 128, N);
     extern __shared__ uint8_t smem_raw[];
     IdxSmem<T> &s = *reinterpret_cast<IdxSmem<T> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -109,17 +127,32 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     ptx::tc_fence_after();
     const uint32_t tmem = s.tmem_base;
 
-    // Walks this CTA's tiles in order; identical in every role.
-    auto tile_at = [&](long i, int &cached_b, int &cached_nv) {
-        TileInfo ti;
-        ti.b = (int)(i / n_tiles);
-        ti.c0 = (int)(i % n_tiles) * kTileKeys;
-        if (ti.b != cached_b) {
-            cached_b = ti.b;
-            cached_nv = seq_visible_max(q_pos, n_comp, ti.b, T, m, Ncap);
+    // Walks this CTA's tiles in order, identically in every role, without a
+    // division per tile: sequence b, tile t within it, visible keys nv of b.
+    struct Walk {
+        int b, t, nv;
+    };
+    auto walk_start = [&]() {
+        Walk w{0, 0, 0};
+        if (t_begin < t_end) {
+            w.b = (int)(t_begin / n_tiles);
+            w.t = (int)(t_begin - (long)w.b * n_tiles);
+            w.nv = seq_visible_max(q_pos, n_comp, w.b, T, m, Ncap);
         }
-        ti.skip = ti.c0 >= cached_nv;
+        return w;
+    };
+    auto walk_info = [&](const Walk &w) {
+        TileInfo ti;
+        ti.b = w.b;
+        ti.c0 = w.t * kTileKeys;
+        ti.skip = ti.c0 >= w.nv;
         return ti;
+    };
+    auto walk_next = [&](Walk &w) {
+        if (++w.t == n_tiles) {
+            w.t = 0;
+            if (++w.b < B) w.nv = seq_visible_max(q_pos, n_comp, w.b, T, m, Ncap);
+        }
     };
     auto fail = [&]() {
         report_error(err, CSA_ERR_TIMEOUT);
@@ -132,16 +165,17 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        int cb = -1, cnv = 0, active_b = -1;
+        int active_b = -1;
         uint32_t j = 0, u = 0;  // tiles loaded, query slots filled
+        Walk w = walk_start();
         const uint64_t policy = ptx::l2_policy_evict_first();
         if (lane == 0) {
             ptx::prefetch_tensormap(&kmap);
             ptx::prefetch_tensormap(&qmap);
         }
         bool ok = true;
-        for (long i = t_begin; i < t_end && ok; ++i) {
-            const TileInfo ti = tile_at(i, cb, cnv);
+        for (long i = t_begin; i < t_end && ok; ++i, walk_next(w)) {
+            const TileInfo ti = walk_info(w);
             if (ti.skip) continue;
             if (ti.b != active_b) {
                 active_b = ti.b;
@@ -172,11 +206,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             wait(&s.q_full[q & 1], (q >> 1) & 1);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        int cb = -1, cnv = 0, active_b = -1;
+        int active_b = -1;
         uint32_t j = 0, u = 0, a = 0;
         bool ok = true;
-        for (long i = t_begin; i < t_end && ok; ++i) {
-            const TileInfo ti = tile_at(i, cb, cnv);
+        Walk w = walk_start();
+        for (long i = t_begin; i < t_end && ok; ++i, walk_next(w)) {
+            const TileInfo ti = walk_info(w);
             if (ti.skip) continue;
             if (ti.b != active_b) {
                 if (active_b >= 0 && lane == 0) ptx::mma_commit(&s.q_empty[(u - 1) & 1]);
@@ -193,9 +228,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 const uint32_t a_base = ptx::smem_u32(s.keys[st]);
                 const uint32_t b_base = ptx::smem_u32(s.q[(u - 1) & 1]);
 #pragma unroll
-                for (int kk = 0; kk < kIdxDim / 32; ++kk)
-                    ptx::mma_f8f6f4(tmem + buf * N, ptx::desc_kmajor_sw128(a_base + kk * 32),
-                                    ptx::desc_kmajor_sw128(b_base + kk * 32), kIdesc, kk > 0 ? 1u : 0u);
+                for (int hm = 0; hm < kHalves; ++hm)
+#pragma unroll
+                    for (int kk = 0; kk < kIdxDim / 32; ++kk)
+                        ptx::mma_f8f6f4(tmem + buf * kAccCols + hm * N,
+                                        ptx::desc_kmajor_sw128(a_base + hm * 128 * kIdxDim + kk * 32),
+                                        ptx::desc_kmajor_sw128(b_base + kk * 32), kIdesc, kk > 0 ? 1u : 0u);
                 ptx::mma_commit(&s.empty[st]);
                 ptx::mma_commit(&s.acc_full[buf]);
             }
@@ -217,36 +255,46 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         const int group = (warp - 2) >> 2;
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const int row = quarter * 32 + lane;
-        int cb = -1, cnv = 0, active_b = -1;
+        int active_b = -1;
         uint32_t u = 0, a = 0;
         int nvis[T];
         // key scales of the group's next own tile are fetched while the
         // current one is processed (their HBM latency overlaps two tiles)
-        int pb = -1, pnv = 0;
+        Walk pw = walk_start();
         long pi = t_begin;
         uint32_t pa = 0;
-        auto fetch_next_own = [&]() -> float {
+        // (thread `row` owns key c0 + 128 hm + row of every tile, hm < kHalves)
+        float sk_next[kHalves];
+        auto fetch_next_own = [&]() {
+#pragma unroll
+            for (int hm = 0; hm < kHalves; ++hm) sk_next[hm] = 0.f;
             while (pi < t_end) {
-                const TileInfo ti = tile_at(pi, pb, pnv);
+                const TileInfo ti = walk_info(pw);
                 ++pi;
+                walk_next(pw);
                 if (ti.skip) continue;
                 const bool own = (pa & 1u) == (uint32_t)group;
                 ++pa;
                 if (!own) continue;
-                const int c = ti.c0 + row;
-                return c < Ncap ? __ldg(k_scale + (size_t)ti.b * Ncap + c) : 0.f;
+#pragma unroll
+                for (int hm = 0; hm < kHalves; ++hm) {
+                    const int c = ti.c0 + 128 * hm + row;
+                    sk_next[hm] = c < Ncap ? __ldg(k_scale + (size_t)ti.b * Ncap + c) : 0.f;
+                }
+                return;
             }
-            return 0.f;
         };
-        float sk_next = fetch_next_own();
+        fetch_next_own();
         bool ok = true;
-        for (long i = t_begin; i < t_end && ok; ++i) {
-            const TileInfo ti = tile_at(i, cb, cnv);
-            const int c = ti.c0 + row;
-            float *lrow = logits + (size_t)ti.b * T * Ncap + c;
+        Walk w = walk_start();
+        for (long i = t_begin; i < t_end && ok; ++i, walk_next(w)) {
+            const TileInfo ti = walk_info(w);
+            float *lrow = logits + (size_t)ti.b * T * Ncap + ti.c0 + row;
             if (ti.skip) {
-                if ((i & 1) == group && c < Ncap)
-                    for (int t = 0; t < T; ++t) lrow[(size_t)t * Ncap] = -INFINITY;
+                if ((i & 1) == group)
+                    for (int hm = 0; hm < kHalves; ++hm)
+                        if (ti.c0 + 128 * hm + row < Ncap)
+                            for (int t = 0; t < T; ++t) lrow[(size_t)t * Ncap + 128 * hm] = -INFINITY;
                 continue;
             }
             if (ti.b != active_b) {
@@ -259,17 +307,21 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
             const uint32_t my_a = a++;
             if ((my_a & 1u) != (uint32_t)group) continue;
-            const float sk = sk_next;
-            sk_next = fetch_next_own();
+            float sk[kHalves];
+#pragma unroll
+            for (int hm = 0; hm < kHalves; ++hm) sk[hm] = sk_next[hm];
+            fetch_next_own();
             const int buf = my_a % kAcc;
             if (!wait(&s.acc_full[buf], (my_a / kAcc) & 1)) { fail(); ok = false; break; }
             ptx::tc_fence_after();
             const float *ws = s.ws[(u - 1) & 1];
-            float acc[T];
+            float acc[kHalves][T];
 #pragma unroll
-            for (int t = 0; t < T; ++t) {
+            for (int ht = 0; ht < kHalves * T; ++ht) {
+                const int hm = ht / T, t = ht % T;
                 uint32_t r0[32], r1[32];
-                const uint32_t col = tmem + ((uint32_t)(quarter * 32) << 16) + buf * N + t * kIdxHeads;
+                const uint32_t col =
+                    tmem + ((uint32_t)(quarter * 32) << 16) + buf * kAccCols + hm * N + t * kIdxHeads;
                 ptx::tmem_ld32(col, r0);
                 ptx::tmem_ld32(col + 32, r1);
                 ptx::tmem_ld_wait();
@@ -287,14 +339,19 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     s2 = fmaf(wb.z, fmaxf(__uint_as_float(r1[4 * h4 + 2]), 0.f), s2);
                     s3 = fmaf(wb.w, fmaxf(__uint_as_float(r1[4 * h4 + 3]), 0.f), s3);
                 }
-                acc[t] = (s0 + s1) + (s2 + s3);
+                acc[hm][t] = (s0 + s1) + (s2 + s3);
             }
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&s.acc_empty[buf]);
-            if (c < Ncap) {
 #pragma unroll
-                for (int t = 0; t < T; ++t) lrow[(size_t)t * Ncap] = c < nvis[t] ? acc[t] * sk : -INFINITY;
+            for (int hm = 0; hm < kHalves; ++hm) {
+                const int c = ti.c0 + 128 * hm + row;
+                if (c < Ncap) {
+#pragma unroll
+                    for (int t = 0; t < T; ++t)
+                        lrow[(size_t)t * Ncap + 128 * hm] = c < nvis[t] ? acc[hm][t] * sk[hm] : -INFINITY;
+                }
             }
         }
         if (ok && active_b >= 0 && lane == 0) ptx::mbar_arrive(&s.q_empty[(u - 1) & 1]);
@@ -350,14 +407,15 @@ template <int T>
 cudaError_t launch_t(const uint8_t *q_idx, const float *q_scale, const float *w_idx, const uint8_t *k_idx,
                      const float *k_scale, const int32_t *q_pos, const int32_t *n_comp, int B, int Ncap, int m,
                      float *logits, int *err, cudaStream_t stream) {
+    using C = IdxCfg<T>;
     CUtensorMap kmap, qmap;
-    if (!make_rows128_map(&kmap, k_idx, (uint64_t)B * Ncap, kTileKeys) ||
+    if (!make_rows128_map(&kmap, k_idx, (uint64_t)B * Ncap, C::kTileKeys) ||
         !make_rows128_map(&qmap, q_idx, (uint64_t)B * T * kIdxHeads, T * kIdxHeads))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(IdxSmem<T>) + 1024;
     cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const long tiles = (long)B * ((Ncap + kTileKeys - 1) / kTileKeys);
+    const long tiles = (long)B * ((Ncap + C::kTileKeys - 1) / C::kTileKeys);
     const int grid = (int)std::min<long>(tiles, num_sms());
     count_launch();
     indexer_tc_kernel<T><<<grid, kThreads, smem, stream>>>(kmap, qmap, q_scale, w_idx, k_scale, q_pos, n_comp, B,
