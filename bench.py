@@ -320,7 +320,7 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3xe4m3->f32 indexer; f32 attention",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3xe4m3->f32 indexer; bf16xbf16->f32 attention",
         "data": "synthetic (seeded N(0,1) latents/queries, FP8 E4M3 per-block scales; no weights needed)",
         "config": {"workload": name, "batch": wl.B, "tokens_per_seq": wl.T, "context_tokens": wl.ctx,
                    "compressed_entries": wl.ncap, "m": wl.m, "topk": wl.k, "swa": wl.W,
@@ -397,7 +397,7 @@ def run_e2e(args, csd, copies, runners, stream, dev, world):
 def kernel_hash() -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("indexer.cu", "common.cuh"):
+    for f in ("indexer.cu", "common.cuh", "ptx.cuh"):
         h.update(open(os.path.join(ROOT, "compressed_sparse_decode_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
