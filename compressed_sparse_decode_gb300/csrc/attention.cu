@@ -30,8 +30,9 @@
 //     0..255 ("lo") and 256..511 ("hi"), each double-buffered: the half this
 //     CTA does not output is released as soon as QK has read it, its own half
 //     after PV.
-// Warps: 0 record-pointer producer, 1 MMA issuer (and TMEM owner), 2-9
-// load + dequantise, 10-13 softmax / epilogue (thread = head). The running max
+// Warps: a record-pointer producer, the MMA issuer (and TMEM owner), 8
+// load + dequantise warps and 4 softmax / epilogue warps (thread = head); see
+// warp_role for the placement on the four schedulers. The running max
 // is rescaled lazily (only when it grows by more than 2^8), in the log2
 // domain. With one split per query the CTAs write the BF16 output and LSE;
 // with several, each split writes a normalised BF16 partial and (max, sum),
@@ -53,7 +54,7 @@ constexpr int kHalf = 256;                  // output latent dims per CTA
 constexpr int kQTmemDims = 384;             // Q dims held in TMEM; the rest in shared memory
 constexpr int kPtrRing = 8;                 // chunks of resolved record pointers
 constexpr int kBatch = 4;                   // chunks whose indices the producer loads at once
-constexpr int kThreads = 448;               // 14 warps
+constexpr int kThreads = 480;               // 15 warps (roles: see warp_role)
 constexpr int kAtom = kChunk * 128;         // one 64-dim column block of X: 64 rows x 128 B
 constexpr int kXHalfBytes = 4 * kAtom;      // 256 dims, 32 KB
 constexpr int kOwnBufs = 2;                 // buffers of the X half a CTA outputs (held until PV)
@@ -186,14 +187,32 @@ __device__ __forceinline__ uint4 *sw128(uint8_t *block, int row, int cc) {
 //   softmax:   reads S(j) and the mask, releases S, writes P(j) once PV(j-1)
 //              is done
 // QK(j) completion frees x_oth[j % 2]; PV(j) completion frees x_own[j % 2] and P.
+// Warp roles. A warp's scheduler is warp % 4, and the softmax warps must
+// cover the four TMEM lane quarters (warp % 4 = 0..3). The MMA issuer shares
+// its scheduler only with the light pointer producer and one softmax warp:
+// tcgen05.mma issue slows down markedly next to two dequantise warps.
+//   scheduler 0: dequantise 0, 4, 8   softmax 12
+//   scheduler 1: MMA 1, producer 5     softmax 13   (warp 9 idle)
+//   scheduler 2: dequantise 2, 6, 10  softmax 14
+//   scheduler 3: dequantise 3, 7      softmax 11
+enum WarpRole { kRoleProducer, kRoleMma, kRoleConvert, kRoleSoftmax, kRoleIdle };
+__device__ __forceinline__ int warp_role(int w) {
+    if (w == 5) return kRoleProducer;
+    if (w == 1) return kRoleMma;
+    if (w == 9) return kRoleIdle;
+    return w >= 11 ? kRoleSoftmax : kRoleConvert;
+}
+// index 0..7 of a dequantise warp
+__device__ __forceinline__ int convert_index(int w) { return w == 0 ? 0 : (w < 5 ? w - 1 : (w < 9 ? w - 2 : 7)); }
+
 __global__ void __launch_bounds__(kThreads, 1)
 attention_tc_kernel(const AttParams P) {
     extern __shared__ uint8_t smem_raw[];
     AttSmem &s = *reinterpret_cast<AttSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int role = warp_role(warp);
     const int rank = blockIdx.x & 1;  // output half: 0 = lo, 1 = hi
     volatile int *abort = &s.abort_flag;
-    const Unit u = make_unit(P);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kPtrRing; ++i) {
@@ -223,6 +242,8 @@ attention_tc_kernel(const AttParams P) {
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = s.tmem_base;
+    ptx::griddep_wait();               // the top-k output (previous kernel in the stream) is complete
+    const Unit u = make_unit(P);
 
     auto fail = [&]() {
         report_error(P.err, CSA_ERR_TIMEOUT);
@@ -232,7 +253,7 @@ attention_tc_kernel(const AttParams P) {
         return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort, kWaitNs)) != 0;
     };
 
-    if (warp == 0) {
+    if (role == kRoleProducer) {
         // ------------------------------------------------------------ record-pointer producer
         // Candidate indices are loaded one batch (4 chunks) ahead; lane L holds
         // candidates L and L + 32 of each chunk of the batch.
@@ -283,7 +304,7 @@ attention_tc_kernel(const AttParams P) {
                 ++j;
             }
         }
-    } else if (warp == 1) {
+    } else if (role == kRoleMma) {
         // ------------------------------------------------------------ MMA issuer
         constexpr uint32_t kIdescQK = ptx::idesc_f32acc(1, 1, 128, kChunk);
         constexpr uint32_t kIdescPV = ptx::idesc_f32acc(1, 1, 128, kHalf, 1);
@@ -367,9 +388,9 @@ attention_tc_kernel(const AttParams P) {
         }
         __syncwarp();
         wait(&s.mma_done, 0);
-    } else if (warp < 2 + kConvWarps) {
+    } else if (role == kRoleConvert) {
         // ------------------------------------------------------------ load + dequantise
-        const int ct = threadIdx.x - 64;  // 0..255
+        const int ct = convert_index(warp) * 32 + lane;  // 0..255
         const int row = ct >> 2, hq = ct & 3;
         const int own_hf = rank, oth_hf = rank ^ 1;
         auto fetch_ptr = [&](int jj, const uint8_t *&rec) -> bool {
@@ -471,7 +492,7 @@ attention_tc_kernel(const AttParams P) {
             ptx::cp_async_commit();
         }
         ptx::cp_async_wait<0>();  // no copy lands after this warp has moved on
-    } else {
+    } else if (role == kRoleSoftmax) {
         // ------------------------------------------------------------ softmax / epilogue
         const int quarter = warp & 3;
         const int h = quarter * 32 + lane;
@@ -605,9 +626,12 @@ attention_tc_kernel(const AttParams P) {
             } else {
                 factor = l > 0.f ? 1.f / l : 0.f;
             }
-            __nv_bfloat16 *dst = (P.n_split == 1)
-                                     ? P.out + ((size_t)r * kHeads + h) * kDim + rank * kHalf
-                                     : P.part_o + (((size_t)r * P.n_split + u.split) * kHeads + h) * kDim + rank * kHalf;
+            // O half -> BF16 rows staged in shared memory (the own X buffers are
+            // free once every PV is done), then each warp writes its 32 head
+            // rows as whole 512-byte rows (one coalesced store per row). Chunk c
+            // (16 B) of row h sits at position c ^ (h & 7): conflict-free both ways.
+            uint8_t *ostage = &s.x_own[0][0];
+            uint8_t *srow = ostage + h * (kHalf * 2);
 #pragma unroll 1
             for (int piece = 0; piece < kHalf / 32; ++piece) {
                 uint32_t o[32];
@@ -618,13 +642,25 @@ attention_tc_kernel(const AttParams P) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = 0u;
                 }
-                uint4 *d4 = reinterpret_cast<uint4 *>(dst + piece * 32);
 #pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    d4[v] = make_uint4(bf16x2_bits(__uint_as_float(o[8 * v + 0]) * factor, __uint_as_float(o[8 * v + 1]) * factor),
-                                       bf16x2_bits(__uint_as_float(o[8 * v + 2]) * factor, __uint_as_float(o[8 * v + 3]) * factor),
-                                       bf16x2_bits(__uint_as_float(o[8 * v + 4]) * factor, __uint_as_float(o[8 * v + 5]) * factor),
-                                       bf16x2_bits(__uint_as_float(o[8 * v + 6]) * factor, __uint_as_float(o[8 * v + 7]) * factor));
+                for (int v = 0; v < 4; ++v) {
+                    const int c = piece * 4 + v;
+                    *reinterpret_cast<uint4 *>(srow + ((c ^ (h & 7)) << 4)) =
+                        make_uint4(bf16x2_bits(__uint_as_float(o[8 * v + 0]) * factor, __uint_as_float(o[8 * v + 1]) * factor),
+                                   bf16x2_bits(__uint_as_float(o[8 * v + 2]) * factor, __uint_as_float(o[8 * v + 3]) * factor),
+                                   bf16x2_bits(__uint_as_float(o[8 * v + 4]) * factor, __uint_as_float(o[8 * v + 5]) * factor),
+                                   bf16x2_bits(__uint_as_float(o[8 * v + 6]) * factor, __uint_as_float(o[8 * v + 7]) * factor));
+                }
+            }
+            __syncwarp();
+            __nv_bfloat16 *dst0 = (P.n_split == 1)
+                                      ? P.out + (size_t)r * kHeads * kDim + rank * kHalf
+                                      : P.part_o + ((size_t)r * P.n_split + u.split) * kHeads * kDim + rank * kHalf;
+#pragma unroll 4
+            for (int i = 0; i < 32; ++i) {
+                const int hr = quarter * 32 + i;  // a head row of this warp
+                const uint4 v = *reinterpret_cast<const uint4 *>(ostage + hr * (kHalf * 2) + ((lane ^ (hr & 7)) << 4));
+                reinterpret_cast<uint4 *>(dst0 + (size_t)hr * kDim)[lane] = v;
             }
             if (rank == 0) {
                 if (P.n_split == 1)
@@ -644,48 +680,78 @@ attention_tc_kernel(const AttParams P) {
 // Folds the per-split normalised partials and the sink:
 //   M = max(sink, m_s), den = e^{sink-M} + sum_s l_s e^{m_s-M},
 //   out = sum_s l_s e^{m_s-M} o_s / den, lse = M + ln den   (log2 domain inside).
+// One warp per (row, head), 16 dims per lane; the (max, sum) pairs and the
+// partial rows of up to 8 splits are loaded together before any use.
+constexpr int kCombineBatch = 8;
 __global__ void __launch_bounds__(256)
 attention_combine_kernel(const __nv_bfloat16 *__restrict__ part_o, const float2 *__restrict__ part_ml,
                          const float *__restrict__ sink, int n_split, __nv_bfloat16 *__restrict__ out,
                          float *__restrict__ lse) {
+    ptx::griddep_wait();  // the split partials (previous kernel in the stream) are complete
     const int r = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.x * 8 + warp;
     const float sk = __ldg(sink + h) * kLog2e;
+    const float2 *ml_row = part_ml + (size_t)r * n_split * kHeads + h;
+    const uint4 *o_row = reinterpret_cast<const uint4 *>(part_o + ((size_t)r * n_split * kHeads + h) * kDim) + lane * 2;
+    const size_t split_stride = (size_t)kHeads * kDim / 8;  // uint4 per split
+    // (every split writes its partial row, zeros when it had no candidates,
+    // so the rows are loaded without waiting for the (max, sum) pairs)
     float M = sk;
-    for (int sp = 0; sp < n_split; ++sp) {
-        const float2 ml = part_ml[((size_t)r * n_split + sp) * kHeads + h];
-        if (ml.y > 0.f) M = fmaxf(M, ml.x);
-    }
-    float den = (sk == -INFINITY) ? 0.f : exp2f(sk - M);
+    if (n_split > kCombineBatch)
+        for (int sp = 0; sp < n_split; ++sp) {
+            const float2 ml = ml_row[(size_t)sp * kHeads];
+            if (ml.y > 0.f) M = fmaxf(M, ml.x);
+        }
+    float den = 0.f;
     float acc[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-    for (int sp = 0; sp < n_split; ++sp) {
-        const float2 ml = part_ml[((size_t)r * n_split + sp) * kHeads + h];
-        if (!(ml.y > 0.f)) continue;
-        const float w = ml.y * exp2f(ml.x - M);
-        den += w;
-        const uint4 *src = reinterpret_cast<const uint4 *>(part_o + (((size_t)r * n_split + sp) * kHeads + h) * kDim) + lane * 2;
+    for (int s0 = 0; s0 < n_split; s0 += kCombineBatch) {
+        float2 ml[kCombineBatch];
+        uint4 v[kCombineBatch][2];
 #pragma unroll
-        for (int v = 0; v < 2; ++v) {
-            const uint4 x = src[v];
-            const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+        for (int q = 0; q < kCombineBatch; ++q) {
+            const int sp = s0 + q;
+            if (sp < n_split) {
+                ml[q] = ml_row[(size_t)sp * kHeads];
+                v[q][0] = o_row[sp * split_stride];
+                v[q][1] = o_row[sp * split_stride + 1];
+            } else {
+                ml[q] = make_float2(0.f, 0.f);
+                v[q][0] = v[q][1] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        if (n_split <= kCombineBatch) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[8 * v + 2 * i] = fmaf(w, bf16_bits_to_float(static_cast<uint16_t>(wv[i] & 0xFFFFu)), acc[8 * v + 2 * i]);
-                acc[8 * v + 2 * i + 1] = fmaf(w, bf16_bits_to_float(static_cast<uint16_t>(wv[i] >> 16)), acc[8 * v + 2 * i + 1]);
+            for (int q = 0; q < kCombineBatch; ++q)
+                if (ml[q].y > 0.f) M = fmaxf(M, ml[q].x);
+        }
+#pragma unroll
+        for (int q = 0; q < kCombineBatch; ++q) {
+            if (!(ml[q].y > 0.f)) continue;
+            const float w = ml[q].y * exp2f(ml[q].x - M);
+            den += w;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const uint32_t wv[4] = {v[q][e].x, v[q][e].y, v[q][e].z, v[q][e].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[8 * e + 2 * i] = fmaf(w, bf16_bits_to_float(static_cast<uint16_t>(wv[i] & 0xFFFFu)), acc[8 * e + 2 * i]);
+                    acc[8 * e + 2 * i + 1] = fmaf(w, bf16_bits_to_float(static_cast<uint16_t>(wv[i] >> 16)), acc[8 * e + 2 * i + 1]);
+                }
             }
         }
     }
+    den += (sk == -INFINITY) ? 0.f : exp2f(sk - M);
     const float inv = den > 0.f ? 1.f / den : 0.f;
     uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)r * kHeads + h) * kDim) + lane * 2;
 #pragma unroll
-    for (int v = 0; v < 2; ++v)
-        dst[v] = make_uint4(bf16x2_bits(acc[8 * v + 0] * inv, acc[8 * v + 1] * inv),
-                            bf16x2_bits(acc[8 * v + 2] * inv, acc[8 * v + 3] * inv),
-                            bf16x2_bits(acc[8 * v + 4] * inv, acc[8 * v + 5] * inv),
-                            bf16x2_bits(acc[8 * v + 6] * inv, acc[8 * v + 7] * inv));
+    for (int e = 0; e < 2; ++e)
+        dst[e] = make_uint4(bf16x2_bits(acc[8 * e + 0] * inv, acc[8 * e + 1] * inv),
+                            bf16x2_bits(acc[8 * e + 2] * inv, acc[8 * e + 3] * inv),
+                            bf16x2_bits(acc[8 * e + 4] * inv, acc[8 * e + 5] * inv),
+                            bf16x2_bits(acc[8 * e + 6] * inv, acc[8 * e + 7] * inv));
     if (lane == 0) lse[(size_t)r * kHeads + h] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
 }
 
@@ -757,13 +823,29 @@ cudaError_t launch_attention(const void *q, const float *sink, float scale, cons
     const size_t smem = sizeof(AttSmem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    // Both kernels may start before their predecessor in the stream ends
+    // (programmatic dependent launch); each waits for it before reading its output.
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * rows * n_split);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
     count_launch();
-    attention_tc_kernel<<<2 * rows * n_split, kThreads, smem, stream>>>(P);
-    e = cudaGetLastError();
+    e = cudaLaunchKernelEx(&cfg, attention_tc_kernel, P);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess || n_split == 1) return e;
+    cfg.gridDim = dim3(kHeads / 8, rows);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
     count_launch();
-    attention_combine_kernel<<<dim3(kHeads / 8, rows), 256, 0, stream>>>(P.part_o, P.part_ml, sink, n_split,
-                                                                         P.out, lse);
+    e = cudaLaunchKernelEx(&cfg, attention_combine_kernel, (const __nv_bfloat16 *)P.part_o,
+                           (const float2 *)P.part_ml, sink, n_split, P.out, lse);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

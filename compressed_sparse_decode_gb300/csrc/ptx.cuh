@@ -319,6 +319,14 @@ __device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gsrc) {
                  : "memory");
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialisation may be set up while its predecessor in the stream finishes;
+// griddep_wait() returns once every prerequisite grid has completed and its
+// memory operations are visible, so it precedes the first read of a
+// predecessor's output. (No early trigger is issued: releasing dependents
+// before a grid's end let them take SMs early and slowed the end-to-end step.)
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Closes this thread's current group of cp.async copies.
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 

@@ -84,6 +84,7 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
     uint32_t *keys = reinterpret_cast<uint32_t *>(smem_raw + sizeof(TopkShared));  // [run][kThreads]
     const int tid = threadIdx.x;
     const uint32_t crank = ptx::cluster_ctarank();
+    ptx::griddep_wait();               // the logits (previous kernel in the stream) are complete and visible
     const int r = blockIdx.x / kCtas;
     const int b = r / T;
     const float *row = logits + (size_t)r * Ncap;
@@ -253,13 +254,15 @@ cudaError_t launch_topk(const float *logits, const int32_t *q_pos, const int32_t
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kCtas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the indexer ends
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     count_launch();
     e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, logits, q_pos, n_comp, T, Ncap, m, k, run, resident, idx_out,
                            cnt_out);
