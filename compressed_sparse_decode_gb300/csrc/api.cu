@@ -25,6 +25,43 @@ cudaError_t launch_attention(const void *, const float *, float, const csa_cache
 namespace csa {
 static std::atomic<uint64_t> g_launches{0};
 void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+namespace {
+constexpr int kMaxDevs = 64;
+int g_sm_count[kMaxDevs];
+struct SmemOptIn {
+    const void *kernel;
+    int dev, bytes;
+};
+SmemOptIn g_smem_opt_in[64];
+int g_n_smem_opt_in;
+std::mutex g_host_cache_mu;
+}  // namespace
+
+int cached_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevs) return 1;
+    std::lock_guard<std::mutex> g(g_host_cache_mu);
+    if (g_sm_count[dev] <= 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        g_sm_count[dev] = n > 0 ? n : 1;
+    }
+    return g_sm_count[dev];
+}
+
+cudaError_t set_max_dynamic_smem_once(const void *kernel, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> g(g_host_cache_mu);
+    for (int i = 0; i < g_n_smem_opt_in; ++i)
+        if (g_smem_opt_in[i].kernel == kernel && g_smem_opt_in[i].dev == dev && g_smem_opt_in[i].bytes >= bytes)
+            return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && g_n_smem_opt_in < 64) g_smem_opt_in[g_n_smem_opt_in++] = {kernel, dev, bytes};
+    return e;
+}
 }  // namespace csa
 
 using namespace csa;

@@ -755,17 +755,10 @@ attention_combine_kernel(const __nv_bfloat16 *__restrict__ part_o, const float2 
     if (lane == 0) lse[(size_t)r * kHeads + h] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
 }
 
-int sm_count() {
-    int dev = 0, n = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n > 0 ? n : 1;
-}
-
 // Splits per query so that about one CTA pair per two SMs is busy.
 int choose_splits(int rows, int max_candidates) {
     const int chunks = (max_candidates + kChunk - 1) / kChunk;
-    const int target = sm_count() / 2;
+    const int target = cached_sm_count() / 2;
     int n = target / (rows > 0 ? rows : 1);
     if (n > chunks) n = chunks;
     return n < 1 ? 1 : n;
@@ -821,7 +814,7 @@ cudaError_t launch_attention(const void *q, const float *sink, float scale, cons
         P.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(ws) + (po + 255) / 256 * 256);
     }
     const size_t smem = sizeof(AttSmem) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_max_dynamic_smem_once(reinterpret_cast<const void *>(attention_tc_kernel), (int)smem);
     if (e != cudaSuccess) return e;
     // Both kernels may start before their predecessor in the stream ends
     // (programmatic dependent launch); each waits for it before reading its output.

@@ -24,6 +24,10 @@ constexpr int kIdxDim = CSA_INDEXER_DIM;
 
 // Host-side count of kernel launches issued by the library.
 void count_launch(int n = 1);
+// Host-side per-device caches (thread-safe): SM count of the current device,
+// and the dynamic shared-memory opt-in of a kernel, set once per device.
+int cached_sm_count();
+cudaError_t set_max_dynamic_smem_once(const void *kernel, int bytes);
 
 // Records first set a sticky code in the per-device error word; the first
 // error wins.

@@ -28,6 +28,8 @@
 // after its copies and MMAs have drained.
 #include <cuda.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -126,6 +128,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = s.tmem_base;
+    // Launched with programmatic stream serialisation: the set-up above may
+    // overlap the previous kernel in the stream, which may have produced any
+    // of the inputs read below.
+    ptx::griddep_wait();
 
     // Walks this CTA's tiles in order, identically in every role, without a
     // division per tile: sequence b, tile t within it, visible keys nv of b.
@@ -396,11 +402,34 @@ bool make_rows128_map(CUtensorMap *map, const void *base, uint64_t rows, uint32_
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int num_sms() {
-    int dev = 0, n = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n > 0 ? n : 1;
+// Encoded maps of recent (base, rows, box) triples, per device: a decode loop
+// calls the indexer with the same few buffers every step, and encoding costs
+// more host time than the launch itself.
+struct MapEntry {
+    const void *base;
+    uint64_t rows;
+    uint32_t box_rows;
+    int dev;
+    CUtensorMap map;
+};
+constexpr int kMapCache = 16;
+MapEntry g_maps[kMapCache];
+int g_map_next;
+std::mutex g_map_mu;
+
+bool cached_rows128_map(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> g(g_map_mu);
+    for (const MapEntry &m : g_maps)
+        if (m.base == base && m.rows == rows && m.box_rows == box_rows && m.dev == dev && base) {
+            *map = m.map;
+            return true;
+        }
+    if (!make_rows128_map(map, base, rows, box_rows)) return false;
+    g_maps[g_map_next] = {base, rows, box_rows, dev, *map};
+    g_map_next = (g_map_next + 1) % kMapCache;
+    return true;
 }
 
 template <int T>
@@ -409,17 +438,28 @@ cudaError_t launch_t(const uint8_t *q_idx, const float *q_scale, const float *w_
                      float *logits, int *err, cudaStream_t stream) {
     using C = IdxCfg<T>;
     CUtensorMap kmap, qmap;
-    if (!make_rows128_map(&kmap, k_idx, (uint64_t)B * Ncap, C::kTileKeys) ||
-        !make_rows128_map(&qmap, q_idx, (uint64_t)B * T * kIdxHeads, T * kIdxHeads))
+    if (!cached_rows128_map(&kmap, k_idx, (uint64_t)B * Ncap, C::kTileKeys) ||
+        !cached_rows128_map(&qmap, q_idx, (uint64_t)B * T * kIdxHeads, T * kIdxHeads))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(IdxSmem<T>) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_max_dynamic_smem_once(reinterpret_cast<const void *>(indexer_tc_kernel<T>), (int)smem);
     if (e != cudaSuccess) return e;
     const long tiles = (long)B * ((Ncap + C::kTileKeys - 1) / C::kTileKeys);
-    const int grid = (int)std::min<long>(tiles, num_sms());
+    const int grid = (int)std::min<long>(tiles, cached_sm_count());
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
     count_launch();
-    indexer_tc_kernel<T><<<grid, kThreads, smem, stream>>>(kmap, qmap, q_scale, w_idx, k_scale, q_pos, n_comp, B,
-                                                            Ncap, m, logits, err);
+    e = cudaLaunchKernelEx(&cfg, indexer_tc_kernel<T>, kmap, qmap, q_scale, w_idx, k_scale, q_pos, n_comp, B, Ncap, m,
+                           logits, err);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

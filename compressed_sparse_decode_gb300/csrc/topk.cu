@@ -247,7 +247,7 @@ cudaError_t launch_topk(const float *logits, const int32_t *q_pos, const int32_t
     const int run = (per_cta + kThreads - 1) / kThreads;
     const int resident = run <= kMaxRun ? 1 : 0;
     const size_t smem = sizeof(TopkShared) + (resident ? (size_t)run * kThreads * sizeof(uint32_t) : 0);
-    cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_max_dynamic_smem_once(reinterpret_cast<const void *>(topk_cluster_kernel), (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(B * T * kCtas);
