@@ -29,7 +29,9 @@ OP_INDEXER, OP_TOPK, OP_ATTENTION, OP_HCA_ATTENTION, OP_DECODE_STEP = range(5)
 EXPORTED = ["csa_workspace_bytes", "csa_indexer_logits", "csa_topk", "csa_gather_swa",
             "csa_sink_attention_decode", "hca_sink_attention_decode", "csa_decode_step",
             "csa_read_device_error", "csa_status_string", "csa_version", "csa_kernel_launches",
-            "csa_sink_attention_decode_noalloc"]
+            "csa_sink_attention_decode_noalloc", "csa_pipeline_staging_bytes", "csa_pipeline_create",
+            "csa_decode_step_host", "csa_pipeline_wait", "csa_pipeline_sync", "csa_pipeline_destroy"]
+PIPELINE_MAX_DEPTH = 4
 
 
 class CsaError(RuntimeError):
@@ -84,6 +86,19 @@ def load(path: str | None = None):
         lib.csa_sink_attention_decode_noalloc.argtypes = ([P, P, f32, csa_cache_desc, P, i32, i32, P, P, P, i32, i32,
                                                            i32, P, P, P])
         lib.csa_sink_attention_decode_noalloc.restype = st
+        lib.csa_pipeline_staging_bytes.argtypes = [i32, i32, i32]
+        lib.csa_pipeline_staging_bytes.restype = sz
+        lib.csa_pipeline_create.argtypes = [C.POINTER(C.c_void_p), i32, i32, i32, P, sz, P]
+        lib.csa_pipeline_create.restype = st
+        lib.csa_decode_step_host.argtypes = ([P] * 9 + [f32, csa_cache_desc, P, i32, i32, P] + [i32] * 3
+                                             + [P, P, P, sz, C.POINTER(C.c_int64)])
+        lib.csa_decode_step_host.restype = st
+        lib.csa_pipeline_wait.argtypes = [P, C.c_int64]
+        lib.csa_pipeline_wait.restype = st
+        lib.csa_pipeline_sync.argtypes = [P]
+        lib.csa_pipeline_sync.restype = st
+        lib.csa_pipeline_destroy.argtypes = [P]
+        lib.csa_pipeline_destroy.restype = st
         lib.csa_read_device_error.argtypes = [C.POINTER(C.c_int32), P]
         lib.csa_read_device_error.restype = st
         _lib = lib
@@ -312,6 +327,104 @@ def csa_decode_step(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q, sink, soft
         _ptr(topk_idx, "topk_idx", torch.int32, (B, T, k)), _ptr(topk_cnt, "topk_cnt", torch.int32, (B, T)),
         _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _stream(stream)), "csa_decode_step")
     return out, lse
+
+
+def _hptr(t: torch.Tensor, name: str, dtype, shape):
+    """Host tensor check for the pipeline: CPU, contiguous, dtype, shape."""
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t.data_ptr()
+
+
+def csa_pipeline_staging_bytes(B: int, T: int, depth: int) -> int:
+    return int(load().csa_pipeline_staging_bytes(B, T, depth))
+
+
+def csa_pipeline_create(B: int, T: int, depth: int, staging: torch.Tensor, stream=None) -> int:
+    """Handle of a new host-I/O pipeline on the current device; ``staging`` is
+    a uint8 device tensor of at least csa_pipeline_staging_bytes(B, T, depth)."""
+    h = C.c_void_p()
+    _check(load().csa_pipeline_create(C.byref(h), B, T, depth, _ptr(staging, "staging", torch.uint8),
+                                      staging.numel(), _stream(stream)), "csa_pipeline_create")
+    return h.value
+
+
+def csa_decode_step_host(pipeline: int, B: int, T: int, h_q_idx, h_q_idx_scale, h_w_idx, h_q, h_q_pos, k_idx,
+                         k_idx_scale, sink, softmax_scale: float, comp: csa_cache_desc, swa_ring, W: int, n_comp,
+                         m: int, k: int, h_out, h_lse, ws) -> int:
+    """Enqueue one step; h_* are host tensors (page-locked for overlap), the
+    rest is the device-resident layer state. Returns the step's ordinal."""
+    Ncap = k_idx.shape[1]
+    R = swa_ring.shape[1]
+    u8 = (torch.uint8, torch.float8_e4m3fn)
+    step = C.c_int64(-1)
+    _check(load().csa_decode_step_host(
+        C.c_void_p(pipeline), _hptr(h_q_idx, "h_q_idx", u8, (B, T, IDX_HEADS, IDX_DIM)),
+        _hptr(h_q_idx_scale, "h_q_idx_scale", torch.float32, (B, T, IDX_HEADS)),
+        _hptr(h_w_idx, "h_w_idx", torch.float32, (B, T, IDX_HEADS)),
+        _hptr(h_q, "h_q", torch.bfloat16, (B, T, HEADS, DIM)), _hptr(h_q_pos, "h_q_pos", torch.int32, (B, T)),
+        _ptr(k_idx, "k_idx", u8, (B, Ncap, IDX_DIM)), _ptr(k_idx_scale, "k_idx_scale", torch.float32, (B, Ncap)),
+        _ptr(sink, "sink", torch.float32, (HEADS,)), float(softmax_scale), comp,
+        _ptr(swa_ring, "swa_ring", torch.uint8, (B, R, RECORD_BYTES)), R, int(W),
+        _ptr(n_comp, "n_comp", torch.int32, (B,)), Ncap, int(m), int(k),
+        _hptr(h_out, "h_out", torch.bfloat16, (B, T, HEADS, DIM)), _hptr(h_lse, "h_lse", torch.float32, (B, T, HEADS)),
+        _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), C.byref(step)), "csa_decode_step_host")
+    return int(step.value)
+
+
+def csa_pipeline_wait(pipeline: int, step: int):
+    _check(load().csa_pipeline_wait(C.c_void_p(pipeline), int(step)), "csa_pipeline_wait")
+
+
+def csa_pipeline_sync(pipeline: int):
+    _check(load().csa_pipeline_sync(C.c_void_p(pipeline)), "csa_pipeline_sync")
+
+
+def csa_pipeline_destroy(pipeline: int):
+    _check(load().csa_pipeline_destroy(C.c_void_p(pipeline)), "csa_pipeline_destroy")
+
+
+class HostPipeline:
+    """Owns a pipeline handle and its device staging area (torch memory).
+    ``step(...)`` enqueues csa_decode_step_host and returns the ordinal;
+    ``wait(i)`` / ``sync()`` block until results are in host memory."""
+
+    def __init__(self, B: int, T: int, depth: int = 2, device=None, stream=None):
+        n = csa_pipeline_staging_bytes(B, T, depth)
+        if n == 0:
+            raise ValueError(f"unsupported pipeline sizes B={B} T={T} depth={depth}")
+        self.B, self.T, self.depth = B, T, depth
+        self.staging = torch.empty(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+        self.handle = csa_pipeline_create(B, T, depth, self.staging, stream)
+
+    def step(self, h_q_idx, h_q_idx_scale, h_w_idx, h_q, h_q_pos, k_idx, k_idx_scale, sink, softmax_scale, comp,
+             swa_ring, W, n_comp, m, k, h_out, h_lse, ws) -> int:
+        return csa_decode_step_host(self.handle, self.B, self.T, h_q_idx, h_q_idx_scale, h_w_idx, h_q, h_q_pos,
+                                    k_idx, k_idx_scale, sink, softmax_scale, comp, swa_ring, W, n_comp, m, k,
+                                    h_out, h_lse, ws)
+
+    def wait(self, step: int):
+        csa_pipeline_wait(self.handle, step)
+
+    def sync(self):
+        csa_pipeline_sync(self.handle)
+
+    def close(self):
+        if self.handle:
+            h, self.handle = self.handle, None
+            csa_pipeline_destroy(h)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def csa_read_device_error(stream=None) -> int:

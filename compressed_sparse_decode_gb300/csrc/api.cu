@@ -114,6 +114,32 @@ bool valid_dims(int B, int T) { return B >= 1 && T >= 1 && T <= CSA_MAX_TOKENS_P
 namespace csa {
 // Error word of the current device, for entry points defined in other files.
 int *error_word_for_current_device() { return device_error_word(); }
+
+// The host-side checks of csa_indexer_logits, csa_topk and
+// csa_sink_attention_decode for the arguments csa_decode_step passes them, so
+// that a bad argument is reported before any of the three launches.
+csa_status_t decode_step_arg_status(const uint8_t *q_idx, const float *q_idx_scale, const float *w_idx,
+                                    const uint8_t *k_idx, const float *k_idx_scale, const void *q, const float *sink,
+                                    float softmax_scale, const csa_cache_desc &comp, const void *swa_ring, int R,
+                                    int W, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap,
+                                    int m, int k, const void *out, const float *lse, const int32_t *topk_idx,
+                                    const void *workspace, size_t workspace_bytes) {
+    if (!valid_dims(B, T) || Ncap < 1 || k < 1 || m < 1) return CSA_ERR_INVALID_ARG;
+    if (!q_idx || !q_idx_scale || !w_idx || !k_idx || !k_idx_scale || !q || !sink || !swa_ring || !q_pos ||
+        !n_comp || !out || !lse)
+        return CSA_ERR_INVALID_ARG;
+    if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(q_idx_scale) || !aligned16(w_idx) ||
+        !aligned16(k_idx_scale) || !aligned16(q) || !aligned16(swa_ring) || !aligned16(out) ||
+        (topk_idx && !aligned16(topk_idx)) || !valid_cache(comp, B))
+        return CSA_ERR_INVALID_ARG;
+    if (W < 1 || W > CSA_MAX_SWA_WINDOW || R < W || !(softmax_scale > 0.f)) return CSA_ERR_INVALID_ARG;
+    if (k > Ncap || k > CSA_MAX_TOPK) return CSA_ERR_UNSUPPORTED;
+    if ((int64_t)B * Ncap >= ((int64_t)1 << 31)) return CSA_ERR_UNSUPPORTED;
+    const size_t need = csa_workspace_bytes(CSA_OP_DECODE_STEP, B, T, Ncap, k);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign))
+        return CSA_ERR_WORKSPACE;
+    return CSA_OK;
+}
 }  // namespace csa
 
 extern "C" {
@@ -229,11 +255,12 @@ csa_status_t csa_decode_step(const uint8_t *q_idx, const float *q_idx_scale, con
                              const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap, int m, int k,
                              void *out, float *lse, int32_t *topk_idx, int32_t *topk_cnt, void *workspace,
                              size_t workspace_bytes, cudaStream_t stream) {
-    if (!valid_dims(B, T) || Ncap < 1 || k < 1) return CSA_ERR_INVALID_ARG;
-    if (k > Ncap || k > CSA_MAX_TOPK) return CSA_ERR_UNSUPPORTED;
-    const size_t need = csa_workspace_bytes(CSA_OP_DECODE_STEP, B, T, Ncap, k);
-    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign))
-        return CSA_ERR_WORKSPACE;
+    // every argument of the three calls is checked before the first launch
+    const csa_status_t a =
+        csa::decode_step_arg_status(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q, sink, softmax_scale, comp,
+                                    swa_ring, R, W, q_pos, n_comp, B, T, Ncap, m, k, out, lse, topk_idx,
+                                    workspace, workspace_bytes);
+    if (a != CSA_OK) return a;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     float *logits = reinterpret_cast<float *>(ws);
     ws += align_up(sizeof(float) * (size_t)B * T * Ncap, kWsAlign);

@@ -28,6 +28,13 @@ void count_launch(int n = 1);
 // and the dynamic shared-memory opt-in of a kernel, set once per device.
 int cached_sm_count();
 cudaError_t set_max_dynamic_smem_once(const void *kernel, int bytes);
+// Every host-side check csa_decode_step makes, before any launch.
+csa_status_t decode_step_arg_status(const uint8_t *q_idx, const float *q_idx_scale, const float *w_idx,
+                                    const uint8_t *k_idx, const float *k_idx_scale, const void *q, const float *sink,
+                                    float softmax_scale, const csa_cache_desc &comp, const void *swa_ring, int R,
+                                    int W, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap,
+                                    int m, int k, const void *out, const float *lse, const int32_t *topk_idx,
+                                    const void *workspace, size_t workspace_bytes);
 
 // Records first set a sticky code in the per-device error word; the first
 // error wins.

@@ -16,9 +16,12 @@
  *
  * Conventions for every call
  *  - Pointers are DEVICE pointers unless stated; the caller owns all memory.
- *    The library allocates nothing. It keeps one device-side error word per
- *    device (see csa_read_device_error) and per-process kernel attributes.
- *  - Calls are asynchronous on `stream`; none synchronises the device.
+ *    The library allocates no device memory (csa_pipeline_create makes a
+ *    small host object, two streams and events). It keeps one device-side
+ *    error word per device (see csa_read_device_error) and per-process kernel
+ *    attributes.
+ *  - Calls are asynchronous on `stream`; none synchronises the device (the
+ *    diagnostics and csa_pipeline_wait/sync/destroy block the host).
  *    Argument errors are detected on the host before any launch and returned
  *    as codes; launch failures return CSA_ERR_CUDA (cudaGetLastError).
  *  - Index or position data that would address memory outside a cache is
@@ -225,6 +228,72 @@ CSA_API csa_status_t csa_decode_step(const uint8_t *q_idx, const float *q_idx_sc
                              int B, int T, int Ncap, int m, int k,
                              void *out, float *lse, int32_t *topk_idx, int32_t *topk_cnt,
                              void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Host-I/O decode pipeline (the pages have no counterpart; it serves callers
+ * whose query-side inputs arrive in, and whose results go back to, host
+ * memory). csa_decode_step_host runs csa_decode_step on per-step copies of
+ * the query-side inputs taken from host memory and copies out/lse back to
+ * host memory. Each step uses one of `depth` staging slots in device memory,
+ * so the host->device copy of step i+1 and the device->host copy of step i-1
+ * run on two copy streams while step i's kernels run on the compute stream;
+ * nothing blocks the host until csa_pipeline_wait / csa_pipeline_sync
+ * ("ROADMAP -- Stage E", section E4: no synchronisation on the decode path).
+ * Results are identical to csa_decode_step on the same inputs.
+ *
+ * csa_pipeline_staging_bytes: device bytes of the staging area for these
+ * sizes (depth slots of q_idx, q_idx_scale, w_idx, q, q_pos, out, lse, each
+ * 256-byte aligned); 0 if an argument is out of range. */
+typedef struct csa_pipeline_s *csa_pipeline_t;
+#define CSA_PIPELINE_MAX_DEPTH 4
+
+CSA_API size_t csa_pipeline_staging_bytes(int B, int T, int depth);
+
+/* Creates a pipeline for B sequences x T tokens on the current device.
+ *   staging   device memory of >= csa_pipeline_staging_bytes(B, T, depth)
+ *             bytes, 256-byte aligned, owned by the caller and untouched by
+ *             anything else while the pipeline lives
+ *   depth     2..CSA_PIPELINE_MAX_DEPTH staging slots
+ *   compute   the caller's stream for the kernels (0 = legacy default)
+ * Allocates the host-side object and creates two non-blocking copy streams
+ * and 3 x depth events on the current device (no device memory). Returns
+ * CSA_ERR_INVALID_ARG for a null handle or staging, a misaligned or short
+ * staging area, or sizes out of range; CSA_ERR_CUDA if a stream or event
+ * cannot be created (nothing is left behind). */
+CSA_API csa_status_t csa_pipeline_create(csa_pipeline_t *pipeline, int B, int T, int depth, void *staging,
+                                         size_t staging_bytes, cudaStream_t compute);
+
+/* Enqueues one decode step. Pointers prefixed h_ are HOST memory with the
+ * layouts of csa_decode_step (q_idx [B,T,64,128] e4m3 codes, q_idx_scale and
+ * w_idx [B,T,64] fp32, q [B,T,128,512] bf16, q_pos [B,T] int32; out
+ * [B,T,128,512] bf16, lse [B,T,128] fp32); page-locked host memory lets the
+ * copies run asynchronously and overlap (pageable memory works, serialised).
+ * The other arguments are the device-resident layer state and sizes of
+ * csa_decode_step (B and T are the pipeline's). The host inputs must stay
+ * unchanged and the host outputs unread until csa_pipeline_wait(step) (or
+ * csa_pipeline_sync) returns. *step_out (may be NULL) receives the step's
+ * ordinal, 0 for the first step of the pipeline. Arguments are checked before
+ * anything is enqueued; CSA_ERR_INVALID_ARG also when the current device is
+ * not the pipeline's. */
+CSA_API csa_status_t csa_decode_step_host(csa_pipeline_t pipeline, const uint8_t *h_q_idx,
+                                          const float *h_q_idx_scale, const float *h_w_idx, const void *h_q,
+                                          const int32_t *h_q_pos, const uint8_t *k_idx, const float *k_idx_scale,
+                                          const float *sink, float softmax_scale, csa_cache_desc comp,
+                                          const void *swa_ring, int R, int W, const int32_t *n_comp, int Ncap,
+                                          int m, int k, void *h_out, float *h_lse, void *workspace,
+                                          size_t workspace_bytes, int64_t *step_out);
+
+/* Blocks the host until step `step` (an ordinal returned by
+ * csa_decode_step_host) has its results in host memory and its host inputs
+ * are no longer read. CSA_ERR_INVALID_ARG for a step not yet enqueued;
+ * CSA_ERR_CUDA if a copy or kernel failed. */
+CSA_API csa_status_t csa_pipeline_wait(csa_pipeline_t pipeline, int64_t step);
+
+/* Blocks the host until every enqueued step has completed. */
+CSA_API csa_status_t csa_pipeline_sync(csa_pipeline_t pipeline);
+
+/* Waits for every enqueued step, then releases the streams, events and host
+ * object (not the staging memory, which the caller owns). NULL is a no-op. */
+CSA_API csa_status_t csa_pipeline_destroy(csa_pipeline_t pipeline);
 
 /* Reads and clears the current device's error word (CSA_OK or the first
  * CSA_ERR_TIMEOUT / CSA_ERR_BAD_INDEX recorded by a kernel). Blocking: it

@@ -83,6 +83,64 @@ def test_host_validation_rejects_before_launch(lib):
                                fake, 1, 1, 10, 4, 4, fake, fake, None, None, None, 0, None) == csd.ERR_WORKSPACE
 
 
+def test_pipeline_staging_sizes(lib):
+    B, T = 32, 1
+    def up(n):
+        return (n + 255) // 256 * 256
+    # q_idx, q_idx_scale, w_idx, q, q_pos, out, lse
+    one = (up(B * T * 64 * 128) + 2 * up(B * T * 64 * 4) + up(B * T * 128 * 512 * 2) + up(B * T * 4)
+           + up(B * T * 128 * 512 * 2) + up(B * T * 128 * 4))
+    assert csd.csa_pipeline_staging_bytes(B, T, 2) == 2 * one
+    assert csd.csa_pipeline_staging_bytes(B, T, 3) == 3 * one
+    assert csd.csa_pipeline_staging_bytes(B, T, 1) == 0          # depth below 2
+    assert csd.csa_pipeline_staging_bytes(B, T, 5) == 0          # depth above the maximum
+    assert csd.csa_pipeline_staging_bytes(B, 5, 2) == 0          # T above the maximum
+    assert csd.csa_pipeline_staging_bytes(0, 1, 2) == 0
+
+
+def test_pipeline_validation_before_any_cuda_call(lib):
+    P = C.c_void_p
+    h = C.c_void_p(0)
+    need = csd.csa_pipeline_staging_bytes(4, 1, 2)
+    assert lib.csa_pipeline_create(None, 4, 1, 2, P(0x1000), need, None) == csd.ERR_INVALID_ARG
+    assert lib.csa_pipeline_create(C.byref(h), 4, 1, 1, P(0x1000), need, None) == csd.ERR_INVALID_ARG
+    assert lib.csa_pipeline_create(C.byref(h), 4, 1, 2, None, need, None) == csd.ERR_INVALID_ARG
+    assert lib.csa_pipeline_create(C.byref(h), 4, 1, 2, P(0x1080), need, None) == csd.ERR_INVALID_ARG  # not 256-aligned
+    assert lib.csa_pipeline_create(C.byref(h), 4, 1, 2, P(0x1000), need - 1, None) == csd.ERR_INVALID_ARG
+    assert h.value is None
+    good = csd.csa_cache_desc()
+    good.base, good.n_records, good.seq_stride, good.seq_capacity = 0x1000, 10, 10, 10
+    fake = P(0x1000)
+    step = C.c_int64(-1)
+    assert lib.csa_decode_step_host(None, *([fake] * 8), C.c_float(0.1), good, fake, 128, 128, fake, 10, 4, 4,
+                                    fake, fake, fake, 1 << 20, C.byref(step)) == csd.ERR_INVALID_ARG
+    assert step.value == -1
+    assert lib.csa_pipeline_wait(None, 0) == csd.ERR_INVALID_ARG
+    assert lib.csa_pipeline_sync(None) == csd.ERR_INVALID_ARG
+    assert lib.csa_pipeline_destroy(None) == csd.OK
+
+
+def test_decode_step_checks_every_argument_before_launching(lib):
+    fake = C.c_void_p(0x1000)
+    good = csd.csa_cache_desc()
+    good.base, good.n_records, good.seq_stride, good.seq_capacity = 0x1000, 10, 10, 10
+    ws = csd.csa_workspace_bytes(csd.OP_DECODE_STEP, 1, 1, 10, 4)
+    args = [fake] * 7 + [C.c_float(0.1), good, fake, 128, 128, fake, fake, 1, 1, 10, 4, 4, fake, fake, None, None,
+                         fake, ws, None]
+    # a null sink (an attention argument) is reported before the indexer launches
+    bad = list(args)
+    bad[6] = None
+    assert lib.csa_decode_step(*bad) == csd.ERR_INVALID_ARG
+    # a window larger than the ring
+    bad = list(args)
+    bad[10] = 64
+    assert lib.csa_decode_step(*bad) == csd.ERR_INVALID_ARG
+    # misaligned output
+    bad = list(args)
+    bad[19] = C.c_void_p(0x1004)
+    assert lib.csa_decode_step(*bad) == csd.ERR_INVALID_ARG
+
+
 def test_product_path_does_not_import_the_oracle():
     pkg = os.path.join(ROOT, "compressed_sparse_decode_gb300")
     for dirpath, _, files in os.walk(pkg):
