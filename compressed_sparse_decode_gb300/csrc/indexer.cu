@@ -9,19 +9,19 @@
 // c >= n_vis(b,t) get -inf ("DSV4 Audit", section A3, item 1).
 //
 // Design (one persistent CTA per SM, 10 warps):
-//   warp 0   TMA producer: 256-key (T <= 2; else 128-key) x 128-byte FP8
-//            tiles (128-byte swizzle) into a 6-stage (8-stage) shared-memory
-//            ring; per sequence, the T*64 query rows (FP8) and the head
-//            weights w*sq into one of two query slots.
-//   warp 1   MMA issuer: tcgen05.mma kind::f8f6f4, M = 128 keys per MMA (two
-//            halves of a 256-key tile), N = 64*T query-head rows, K = 128
-//            (4 x K32), fp32 accumulators in TMEM, up to four tiles deep so the
-//            epilogue overlaps the next tiles.
+//   warp 0   TMA producer: 512-key (T = 1), 256-key (T = 2) or 128-key tiles
+//            of 128-byte FP8 rows (128-byte swizzle, at most 256 rows per
+//            copy) into a 3-, 6- or 8-stage shared-memory ring; per sequence,
+//            the T*64 query rows (FP8) and the head weights w*sq into one of
+//            two query slots.
+//   warp 1   MMA issuer: tcgen05.mma kind::f8f6f4, M = 128 keys per MMA (one
+//            per 128-key block of a tile), N = 64*T query-head rows, K = 128
+//            (4 x K32), fp32 accumulators in TMEM, two or four tiles deep so
+//            the epilogue overlaps the next tiles.
 //   warps 2-9 epilogue, two groups of 4 taking alternate tiles: thread i owns
-//            TMEM lane i = key c0+i of each 128-key half; it reads the 64*T head dot products,
-//            applies ReLU and the head weights, scales by the key's scale and
-//            writes the row of logits (coalesced). Up to four accumulator
-//            buffers let the MMA run ahead of both groups.
+//            TMEM lane i = key c0+128j+i of each 128-key block j; it reads the
+//            64*T head dot products, applies ReLU and the head weights, scales
+//            by the key's scale and writes the row of logits (coalesced).
 // Keys are read once from HBM for all T tokens of a sequence; tiles past the
 // largest visible range of their sequence are never loaded (written -inf).
 // Every wait is bounded; a timeout records CSA_ERR_TIMEOUT and the CTA exits
@@ -41,15 +41,17 @@ constexpr int kThreads = 320;  // producer, MMA, two 4-warp epilogue groups
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
 // Tile shape per tokens-per-sequence T: a tile is kHalves blocks of 128 keys
-// (one M = 128 MMA each); 256-key tiles halve the fixed per-tile costs
-// (barrier waits, commits, bookkeeping) where TMEM still holds four
-// accumulators (T <= 2).
+// (one M = 128 MMA each). The MMA issuer's fixed per-tile cost (waits,
+// commits, bookkeeping) does not grow with the tile, so tiles are as large as
+// two accumulators in TMEM (512 columns) allow: 512 keys at T = 1, 256 at
+// T = 2. The ring holds 192 KB (T <= 2) or 128 KB of keys.
 template <int T>
 struct IdxCfg {
-    static constexpr int kHalves = T <= 2 ? 2 : 1;
+    static constexpr int kHalves = T == 1 ? 4 : (T == 2 ? 2 : 1);
     static constexpr int kTileKeys = 128 * kHalves;
-    static constexpr int kStages = kHalves == 2 ? 6 : 8;
-    static constexpr int kTileBytes = kTileKeys * kIdxDim;  // 32 KB or 16 KB
+    static constexpr int kBoxRows = kTileKeys < 256 ? kTileKeys : 256;  // rows per TMA copy
+    static constexpr int kStages = kHalves == 4 ? 3 : (kHalves == 2 ? 6 : 8);
+    static constexpr int kTileBytes = kTileKeys * kIdxDim;  // 64, 32 or 16 KB
     static constexpr int N = T * kIdxHeads;                 // accumulator columns per 128 keys
     static constexpr int kAccCols = kHalves * N;            // per tile
     static constexpr int kAcc = (4 * kAccCols <= 512) ? 4 : 2;
@@ -200,7 +202,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             if (!wait(&s.empty[st], ((j / kStages) & 1) ^ 1)) { fail(); ok = false; break; }
             if (lane == 0) {
                 ptx::mbar_arrive_expect_tx(&s.full[st], kTileBytes);
-                ptx::tma_load_2d_hint(s.keys[st], &kmap, &s.full[st], 0, ti.b * Ncap + ti.c0, policy);
+#pragma unroll
+                for (int r = 0; r < kTileKeys; r += C::kBoxRows)
+                    ptx::tma_load_2d_hint(s.keys[st] + r * kIdxDim, &kmap, &s.full[st], 0, ti.b * Ncap + ti.c0 + r,
+                                          policy);
             }
             __syncwarp();
             ++j;
@@ -438,7 +443,7 @@ cudaError_t launch_t(const uint8_t *q_idx, const float *q_scale, const float *w_
                      float *logits, int *err, cudaStream_t stream) {
     using C = IdxCfg<T>;
     CUtensorMap kmap, qmap;
-    if (!cached_rows128_map(&kmap, k_idx, (uint64_t)B * Ncap, C::kTileKeys) ||
+    if (!cached_rows128_map(&kmap, k_idx, (uint64_t)B * Ncap, C::kBoxRows) ||
         !cached_rows128_map(&qmap, q_idx, (uint64_t)B * T * kIdxHeads, T * kIdxHeads))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(IdxSmem<T>) + 1024;
