@@ -41,22 +41,22 @@ struct TopkShared {
     int remaining;
 };
 
-// Block-wide exclusive prefix sum of an int; every thread must call it.
-__device__ __forceinline__ int block_exclusive_sum(int v, int *wsum, int &total) {
+// Block-wide exclusive prefix sum of a uint32 (modular); every thread must call it.
+__device__ __forceinline__ uint32_t block_exclusive_sum_u32(uint32_t v, int *wsum, uint32_t &total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = v;
+    uint32_t incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += u;
     }
-    if (lane == 31) wsum[warp] = incl;
+    if (lane == 31) wsum[warp] = (int)incl;
     __syncthreads();
-    int before = 0, all = 0;
+    uint32_t before = 0, all = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-        const int x = wsum[w];
-        before += w < warp ? x : 0;
+        const uint32_t x = (uint32_t)wsum[w];
+        before += w < warp ? x : 0u;
         all += x;
     }
     __syncthreads();
@@ -105,8 +105,22 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
     auto key_j = [&](int j) -> uint32_t {
         return resident ? keys[j * kThreads + tid] : order_key(__ldg(row + mine + j));
     };
-    if (resident)
-        for (int j = 0; j < n_my; ++j) keys[j * kThreads + tid] = order_key(__ldg(row + mine + j));
+    if (resident) {
+        // 16-byte loads where the run is whole and aligned (rows of a multiple
+        // of 4 entries, runs of a multiple of 4), scalar loads otherwise
+        int j = 0;
+        if ((Ncap & 3) == 0 && (run & 3) == 0) {
+            const float4 *r4 = reinterpret_cast<const float4 *>(row + mine);
+            for (; j + 3 < n_my; j += 4) {
+                const float4 v = __ldg(r4 + (j >> 2));
+                keys[(j + 0) * kThreads + tid] = order_key(v.x);
+                keys[(j + 1) * kThreads + tid] = order_key(v.y);
+                keys[(j + 2) * kThreads + tid] = order_key(v.z);
+                keys[(j + 3) * kThreads + tid] = order_key(v.w);
+            }
+        }
+        for (; j < n_my; ++j) keys[j * kThreads + tid] = order_key(__ldg(row + mine + j));
+    }
     for (int i = tid; i < 3 * kBins; i += kThreads) (&s.local[0][0])[i] = 0u;
     __syncthreads();
 
@@ -142,10 +156,14 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
             reinterpret_cast<uint4 *>(s.reduced[pass])[tid] = acc;
             part = (int)(acc.x + acc.y + acc.z + acc.w);
         }
-        int range_tot;
-        block_exclusive_sum(part, s.wsum, range_tot);
+        // this CTA's range total: the partial sums sit in the first per/4 <= 64 threads
+        if (tid < 64) {
+            const int w = (int)__reduce_add_sync(0xffffffffu, (unsigned)part);
+            if ((tid & 31) == 0) s.wsum[tid >> 5] = w;
+        }
+        __syncthreads();
         if (tid < kCtas)
-            st_cluster_s32(ptx::mapa(ptx::smem_u32(&s.range_total[pass][crank]), tid), range_tot);
+            st_cluster_s32(ptx::mapa(ptx::smem_u32(&s.range_total[pass][crank]), tid), s.wsum[0] + s.wsum[1]);
         ptx::cluster_sync();  // every range total has arrived
         // The range holding the `remaining`-th largest matching key (ranges of
         // larger digits first); every CTA reads that range's bins and picks the
@@ -203,9 +221,23 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
         gt += key > prefix;
         eq += key == prefix;
     }
-    int tot_gt, tot_eq;
-    block_exclusive_sum(gt, s.wsum, tot_gt);
-    const int eq_excl = block_exclusive_sum(eq, s.wsum, tot_eq);
+    int gt_excl, eq_excl, tot_gt, tot_eq;
+    if (slice < 65536) {
+        // one scan of (gt << 16 | eq): a CTA holds fewer than 65536 entries,
+        // so the low half never carries into the high half
+        uint32_t tot_packed;
+        const uint32_t excl = block_exclusive_sum_u32(((uint32_t)gt << 16) | (uint32_t)eq, s.wsum, tot_packed);
+        gt_excl = (int)(excl >> 16);
+        eq_excl = (int)(excl & 0xFFFFu);
+        tot_gt = (int)(tot_packed >> 16);
+        tot_eq = (int)(tot_packed & 0xFFFFu);
+    } else {
+        uint32_t t0, t1;
+        gt_excl = (int)block_exclusive_sum_u32((uint32_t)gt, s.wsum, t0);
+        eq_excl = (int)block_exclusive_sum_u32((uint32_t)eq, s.wsum, t1);
+        tot_gt = (int)t0;
+        tot_eq = (int)t1;
+    }
     const uint32_t counts0 = ptx::mapa(ptx::smem_u32(&s.counts[0][0]), 0);
     if (tid == 0) {
         st_cluster_s32(counts0 + crank * 8, tot_gt);
@@ -220,9 +252,10 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
         base += s.peer_counts[c][0] + min(max(remaining - eq_before, 0), ce);
         eq_before += ce;
     }
-    const int take = gt + min(max(remaining - eq_before - eq_excl, 0), eq);
-    int tot_take;
-    int pos = base + block_exclusive_sum(take, s.wsum, tot_take);
+    // keys == K* are taken in index order while the budget lasts, so the
+    // threads before this one took min(budget, eq_excl) of them
+    const int budget = max(remaining - eq_before, 0);
+    int pos = base + gt_excl + min(budget, eq_excl);
     int eq_seen = eq_before + eq_excl;
     for (int j = 0; j < n_my; ++j) {
         const uint32_t key = key_j(j);
