@@ -377,10 +377,11 @@ attention_tc_kernel(const AttParams P) {
             __syncwarp();
             return true;
         };
-        if (ok && u.n_chunks > 0 && !issue_qk(0)) { fail(); ok = false; }
-        for (int j = 0; j < u.n_chunks && ok; ++j) {
-            if (j + 1 < u.n_chunks && !issue_qk(j + 1)) { fail(); ok = false; break; }
-            if (!issue_pv(j)) { fail(); ok = false; break; }
+        // QK(0), then QK(j+1) before PV(j); one call site each keeps a single
+        // copy of the unrolled MMA sequences in the instruction stream
+        for (int j = 0; j <= u.n_chunks && ok; ++j) {
+            if (j < u.n_chunks && !issue_qk(j)) { fail(); ok = false; break; }
+            if (j > 0 && !issue_pv(j - 1)) { fail(); ok = false; break; }
         }
         if (lane == 0) {
             ptx::mma_commit(&s.o_final);
@@ -456,39 +457,32 @@ attention_tc_kernel(const AttParams P) {
         // pending" before each conversion means the half about to be converted
         // has landed.
         bool ok = true;
-        const uint8_t *rec_nxt = nullptr;
-        if (u.n_chunks > 0) {
-            if (!fetch_ptr(0, rec_nxt)) { fail(); ok = false; }
-            if (ok) load_half(oth_hf, rec_nxt);
-            ptx::cp_async_commit();
-            if (ok) load_half(own_hf, rec_nxt);
-            ptx::cp_async_commit();
-        }
-        for (int j = 0; j < u.n_chunks && ok; ++j) {
-            const int ob = j % kOthBufs, wb = j % kOwnBufs;
-            const uint8_t *rec_cur = rec_nxt;
-            // ---- other half of chunk j
-            ptx::cp_async_wait<1>();
-            __syncwarp();  // the row's multipliers (copied by its first thread) are visible to all four
-            if (!wait(&s.oth_empty[ob], ((j / kOthBufs) & 1) ^ 1)) { fail(); ok = false; break; }
-            convert_half(oth_hf, s.x_oth[ob], rec_cur != nullptr);
-            ptx::fence_proxy_async_smem();  // generic-proxy stores -> MMA (async proxy) reads
-            __syncwarp();                   // (and the row's threads are done with the staging)
-            if (lane == 0) ptx::mbar_arrive(&s.oth_full[ob]);
-            if (j + 1 < u.n_chunks) {
-                if (!fetch_ptr(j + 1, rec_nxt)) { fail(); ok = false; break; }
-                load_half(oth_hf, rec_nxt);
+        const uint8_t *rec_nxt = nullptr, *rec_cur = nullptr;
+        if (u.n_chunks > 0 && !fetch_ptr(0, rec_nxt)) { fail(); ok = false; }
+        // Half-steps t = 2j (other half of chunk j) and 2j + 1 (own half): the
+        // staging of half-step t + 2 is copied right after half-step t is
+        // converted, and half-steps -2 and -1 copy chunk 0. One call site per
+        // helper keeps a single copy of each in the instruction stream.
+        for (int t = -2; t < 2 * u.n_chunks && ok; ++t) {
+            const int j = t >> 1;  // (floor: -1 for t = -2, -1)
+            const bool own_step = (t & 1) != 0;
+            const int hf = own_step ? own_hf : oth_hf;
+            if (t >= 0) {
+                if (!own_step) rec_cur = rec_nxt;
+                const int nb = own_step ? kOwnBufs : kOthBufs;
+                uint8_t *xs = own_step ? s.x_own[j % kOwnBufs] : s.x_oth[j % kOthBufs];
+                uint64_t *empty_bar = own_step ? &s.own_empty[j % kOwnBufs] : &s.oth_empty[j % kOthBufs];
+                uint64_t *full_bar = own_step ? &s.own_full[j % kOwnBufs] : &s.oth_full[j % kOthBufs];
+                ptx::cp_async_wait<1>();
+                __syncwarp();  // the row's multipliers (copied by its first thread) are visible to all four
+                if (!wait(empty_bar, ((j / nb) & 1) ^ 1)) { fail(); ok = false; break; }
+                convert_half(hf, xs, rec_cur != nullptr);
+                ptx::fence_proxy_async_smem();  // generic-proxy stores -> MMA (async proxy) reads
+                __syncwarp();                   // (and the row's threads are done with the staging)
+                if (lane == 0) ptx::mbar_arrive(full_bar);
+                if (!own_step && j + 1 < u.n_chunks && !fetch_ptr(j + 1, rec_nxt)) { fail(); ok = false; break; }
             }
-            ptx::cp_async_commit();
-            // ---- own half of chunk j
-            ptx::cp_async_wait<1>();
-            __syncwarp();
-            if (!wait(&s.own_empty[wb], ((j / kOwnBufs) & 1) ^ 1)) { fail(); ok = false; break; }
-            convert_half(own_hf, s.x_own[wb], rec_cur != nullptr);
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&s.own_full[wb]);
-            if (j + 1 < u.n_chunks) load_half(own_hf, rec_nxt);
+            if (j + 1 < u.n_chunks) load_half(hf, rec_nxt);
             ptx::cp_async_commit();
         }
         ptx::cp_async_wait<0>();  // no copy lands after this warp has moved on
