@@ -34,6 +34,7 @@ METRIC = "CSA decode tokens/s at 128K ctx; achieved HBM GB/s and % of roofline"
 UNIT = "tokens/s"
 SCALE = 1.0 / math.sqrt(512)
 N_COPIES = 3  # rotating input copies: each step's inputs are not L2-resident
+IDX_SAMPLE_EVERY = 4  # timed-region steps whose indexer launch is bracketed by events
 
 
 def parse():
@@ -262,9 +263,12 @@ def run_ours(args, rank, world, local_rank):
     clocks.start()
     time.sleep(0.3)
     # Events inside the timed loop bracket only the indexer (the roofline
-    # kernel): an event between two kernels would stop the next one from being
-    # set up while its predecessor drains (programmatic dependent launch).
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # kernel), and only on every IDX_SAMPLE_EVERY-th step: an event between two
+    # kernels stops the next one from being set up while its predecessor
+    # drains (programmatic dependent launch), which costs ~9 us per bracketed
+    # step on the 128K workload.
+    sampled = [i for i in range(args.steps) if i % IDX_SAMPLE_EVERY == 0]
+    ev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for i in sampled}
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # keep the GPU busy right up to the timed region (clock samples stay meaningful)
     with torch.cuda.stream(stream):
@@ -279,10 +283,12 @@ def run_ours(args, rank, world, local_rank):
         start.record(stream)
         for i in range(args.steps):
             r = runners[i % N_COPIES]
-            e0, e1 = ev[i]
-            e0.record(stream)
-            r.indexer()
-            e1.record(stream)
+            if i in ev:
+                ev[i][0].record(stream)
+                r.indexer()
+                ev[i][1].record(stream)
+            else:
+                r.indexer()
             r.topk()
             r.attention()
         end.record(stream)
@@ -293,7 +299,7 @@ def run_ours(args, rank, world, local_rank):
     time.sleep(0.1)
     clocks.stop()
     total_ms = start.elapsed_time(end)
-    t_idx = [a.elapsed_time(b) for a, b in ev]
+    t_idx = [a.elapsed_time(b) for a, b in ev.values()]
     # per-kernel breakdown (after the timed region, same inputs): events around
     # every kernel, which serialises their boundaries
     bev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(min(args.steps, 12))]
@@ -336,8 +342,9 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world}"},
         "kernel_ms": {"indexer": round(idx_ms, 5), "topk": round(statistics.mean(t_topk), 5),
                       "attention": round(statistics.mean(t_att), 5),
-                      "source": "indexer: events in the timed region; topk, attention (+ split combine): "
-                                "a breakdown pass after it with events around every kernel"},
+                      "source": f"indexer: events around every {IDX_SAMPLE_EVERY}th launch in the timed region "
+                                f"({len(t_idx)} launches); topk, attention (+ split combine): a breakdown pass "
+                                "after it with events around every kernel"},
         "roofline": {"kernel": "csa_indexer_logits", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "peak_source": peaks["source"], "traffic": traffic, "algorithmic_bytes": idx_bytes},

@@ -337,25 +337,31 @@ attention_tc_kernel(const AttParams P) {
         using Hi = std::integral_constant<int, 1>;
         // QK(jq) -> S once the softmax has read S(jq-1): the half this CTA does
         // not output first (it is converted first), then its own half.
+        // QK(jq): the half this CTA does not output first (its buffer is
+        // released as soon as these MMAs complete), then its own half. The
+        // two parts share one instance of each templated half (rank 0 runs Hi
+        // then Lo, rank 1 Lo then Hi), so the unrolled MMA sequences appear
+        // once each in the instruction stream.
         auto issue_qk = [&](int jq) -> bool {
             const int ob = jq % kOthBufs, wb = jq % kOwnBufs;
-            if (!wait(&s.oth_full[ob], (jq / kOthBufs) & 1)) return false;
-            if (jq >= 1 && !wait(&s.s_free, (jq - 1) & 1)) return false;
-            ptx::tc_fence_after();
-            if (lane == 0) {
-                if (rank == 0) qk_half(Hi{}, s.x_oth[ob], true);
-                else qk_half(Lo{}, s.x_oth[ob], true);
-                ptx::mma_commit(&s.oth_empty[ob]);
+#pragma unroll 1
+            for (int part = 0; part < 2; ++part) {
+                const bool oth_part = part == 0;
+                if (oth_part) {
+                    if (!wait(&s.oth_full[ob], (jq / kOthBufs) & 1)) return false;
+                    if (jq >= 1 && !wait(&s.s_free, (jq - 1) & 1)) return false;
+                } else {
+                    if (!wait(&s.own_full[wb], (jq / kOwnBufs) & 1)) return false;
+                }
+                ptx::tc_fence_after();
+                if (lane == 0) {
+                    const uint8_t *xbuf = oth_part ? s.x_oth[ob] : s.x_own[wb];
+                    if ((rank == 0) == oth_part) qk_half(Hi{}, xbuf, oth_part);
+                    else qk_half(Lo{}, xbuf, oth_part);
+                    ptx::mma_commit(oth_part ? &s.oth_empty[ob] : &s.s_full);
+                }
+                __syncwarp();
             }
-            __syncwarp();
-            if (!wait(&s.own_full[wb], (jq / kOwnBufs) & 1)) return false;
-            ptx::tc_fence_after();
-            if (lane == 0) {
-                if (rank == 0) qk_half(Lo{}, s.x_own[wb], false);
-                else qk_half(Hi{}, s.x_own[wb], false);
-                ptx::mma_commit(&s.s_full);
-            }
-            __syncwarp();
             return true;
         };
         auto issue_pv = [&](int jp) -> bool {
@@ -403,17 +409,22 @@ attention_tc_kernel(const AttParams P) {
             return true;
         };
         // copies this thread's pieces of half hf of record `rec` into the half's staging
+        // Records are read by the two CTAs of a pair within a chunk of each
+        // other and never again: evict-first keeps them from displacing what
+        // the next kernels read (measured: the next step's indexer runs
+        // 0.7 us faster, this kernel 1 us faster).
+        const uint64_t rec_policy = ptx::l2_policy_evict_first();
         auto load_half = [&](int hf, const uint8_t *rec) {
             if (!rec) return;
             if (hf == 0) {
 #pragma unroll
-                for (int i = 0; i < kLoPieces; ++i) ptx::cp_async_16(&s.stage_lo.piece[i][ct], rec + 16 * (hq + 4 * i));
-                if (hq == 0) ptx::cp_async_16(&s.stage_lo.scale[row], rec + kScaleOffset);
+                for (int i = 0; i < kLoPieces; ++i) ptx::cp_async_16_hint(&s.stage_lo.piece[i][ct], rec + 16 * (hq + 4 * i), rec_policy);
+                if (hq == 0) ptx::cp_async_16_hint(&s.stage_lo.scale[row], rec + kScaleOffset, rec_policy);
             } else {
 #pragma unroll
                 for (int i = 0; i < kHiPieces; ++i)
-                    ptx::cp_async_16(&s.stage_hi.piece[i][ct], rec + 256 + 16 * (hq + 4 * i));
-                if (hq == 0) ptx::cp_async_16(&s.stage_hi.scale[row], rec + kScaleOffset);
+                    ptx::cp_async_16_hint(&s.stage_hi.piece[i][ct], rec + 256 + 16 * (hq + 4 * i), rec_policy);
+                if (hq == 0) ptx::cp_async_16_hint(&s.stage_hi.scale[row], rec + kScaleOffset, rec_policy);
             }
         };
         // Piece hq + 4 i of a half: code pieces hold 16 dims starting at

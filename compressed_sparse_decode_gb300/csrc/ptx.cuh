@@ -313,6 +313,13 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t re
 
 
 // 16-byte global -> shared copy through the load/store path (L1 bypassed).
+// The same with an L2 cache policy (e.g. l2_policy_evict_first()).
+__device__ __forceinline__ void cp_async_16_hint(void *smem_dst, const void *gsrc, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
+                 "l"(reinterpret_cast<uint64_t>(gsrc)), "l"(policy)
+                 : "memory");
+}
+
 __device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gsrc) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
                  "l"(reinterpret_cast<uint64_t>(gsrc))
