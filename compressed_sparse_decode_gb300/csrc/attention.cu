@@ -53,7 +53,7 @@ constexpr int kChunk = 64;                  // candidates per chunk
 constexpr int kHalf = 256;                  // output latent dims per CTA
 constexpr int kQTmemDims = 384;             // Q dims held in TMEM; the rest in shared memory
 constexpr int kPtrRing = 8;                 // chunks of resolved record pointers
-constexpr int kBatch = 4;                   // chunks whose indices the producer loads at once
+constexpr int kIdxAhead = 4;                // chunks ahead whose candidate indices the producer has loaded
 constexpr int kThreads = 480;               // 15 warps (roles: see warp_role)
 constexpr int kAtom = kChunk * 128;         // one 64-dim column block of X: 64 rows x 128 B
 constexpr int kXHalfBytes = 4 * kAtom;      // 256 dims, 32 KB
@@ -255,54 +255,54 @@ attention_tc_kernel(const AttParams P) {
 
     if (role == kRoleProducer) {
         // ------------------------------------------------------------ record-pointer producer
-        // Candidate indices are loaded one batch (4 chunks) ahead; lane L holds
-        // candidates L and L + 32 of each chunk of the batch.
-        auto load_raw = [&](int g, int (&raw)[2 * kBatch]) {
-#pragma unroll
-            for (int q = 0; q < 2 * kBatch; ++q) {
-                const int i = u.cb + g * kBatch * kChunk + q * 32 + lane;
-                raw[q] = (!P.hca && i < u.ce && i < u.n_sel) ? __ldg(P.topk_idx + (size_t)u.r * P.k + i) : i;
-            }
+        // Candidate indices are loaded kIdxAhead chunks ahead; lane L holds
+        // candidates L and L + 32 of a chunk. A rolled loop keeps this warp's
+        // code small: it shares an instruction cache with the MMA issuer.
+        auto load_raw = [&](int jj, int &r0, int &r1) {
+            const int i0 = u.cb + jj * kChunk + lane, i1 = i0 + 32;
+            const int32_t *src = P.topk_idx + (size_t)u.r * P.k;
+            r0 = (!P.hca && i0 < u.ce && i0 < u.n_sel) ? __ldg(src + i0) : i0;
+            r1 = (!P.hca && i1 < u.ce && i1 < u.n_sel) ? __ldg(src + i1) : i1;
         };
-        const int n_batches = (u.n_chunks + kBatch - 1) / kBatch;
-        int cur[2 * kBatch], nxt[2 * kBatch];
-        if (n_batches > 0) load_raw(0, nxt);
-        int j = 0;
+        int ahead[kIdxAhead][2];
+#pragma unroll
+        for (int q = 0; q < kIdxAhead; ++q)
+            if (q < u.n_chunks) load_raw(q, ahead[q][0], ahead[q][1]);
         bool ok = true;
-        for (int g = 0; g < n_batches && ok; ++g) {
+#pragma unroll 1
+        for (int j = 0; j < u.n_chunks && ok; ++j) {
+            const int raw[2] = {ahead[0][0], ahead[0][1]};
 #pragma unroll
-            for (int q = 0; q < 2 * kBatch; ++q) cur[q] = nxt[q];
-            if (g + 1 < n_batches) load_raw(g + 1, nxt);
-#pragma unroll
-            for (int cc = 0; cc < kBatch; ++cc) {
-                if (j >= u.n_chunks) break;
-                const int pr = j % kPtrRing;
-                if (!wait(&s.ptr_empty[pr], ((j / kPtrRing) & 1) ^ 1)) { fail(); ok = false; break; }
-                bool valid[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int i = u.cb + j * kChunk + e * 32 + lane;
-                    const uint8_t *rec = nullptr;
-                    if (i < u.ce) {
-                        if (i < u.n_sel) {
-                            const int64_t ri = record_index(P.comp, u.b, cur[2 * cc + e]);
-                            if (ri >= 0) rec = P.comp.base + ri * kRecBytes;
-                            else if (rank == 0) report_error(P.err, CSA_ERR_BAD_INDEX);
-                        } else {
-                            const int pos = u.j0 + (i - u.n_sel);
-                            rec = P.ring + ((int64_t)u.b * P.R + pos % P.R) * kRecBytes;
-                        }
-                    }
-                    valid[e] = rec != nullptr;
-                    s.rec[pr][e * 32 + lane] = rec;
-                }
-                const uint32_t m0 = __ballot_sync(0xffffffffu, valid[0]);
-                const uint32_t m1 = __ballot_sync(0xffffffffu, valid[1]);
-                if (lane == 0) s.vmask[pr] = (uint64_t)m0 | ((uint64_t)m1 << 32);
-                __syncwarp();
-                ptx::mbar_arrive(&s.ptr_full[pr]);
-                ++j;
+            for (int q = 0; q + 1 < kIdxAhead; ++q) {
+                ahead[q][0] = ahead[q + 1][0];
+                ahead[q][1] = ahead[q + 1][1];
             }
+            if (j + kIdxAhead < u.n_chunks) load_raw(j + kIdxAhead, ahead[kIdxAhead - 1][0], ahead[kIdxAhead - 1][1]);
+            const int pr = j % kPtrRing;
+            if (!wait(&s.ptr_empty[pr], ((j / kPtrRing) & 1) ^ 1)) { fail(); ok = false; break; }
+            bool valid[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int i = u.cb + j * kChunk + e * 32 + lane;
+                const uint8_t *rec = nullptr;
+                if (i < u.ce) {
+                    if (i < u.n_sel) {
+                        const int64_t ri = record_index(P.comp, u.b, raw[e]);
+                        if (ri >= 0) rec = P.comp.base + ri * kRecBytes;
+                        else if (rank == 0) report_error(P.err, CSA_ERR_BAD_INDEX);
+                    } else {
+                        const int pos = u.j0 + (i - u.n_sel);
+                        rec = P.ring + ((int64_t)u.b * P.R + pos % P.R) * kRecBytes;
+                    }
+                }
+                valid[e] = rec != nullptr;
+                s.rec[pr][e * 32 + lane] = rec;
+            }
+            const uint32_t m0 = __ballot_sync(0xffffffffu, valid[0]);
+            const uint32_t m1 = __ballot_sync(0xffffffffu, valid[1]);
+            if (lane == 0) s.vmask[pr] = (uint64_t)m0 | ((uint64_t)m1 << 32);
+            __syncwarp();
+            ptx::mbar_arrive(&s.ptr_full[pr]);
         }
     } else if (role == kRoleMma) {
         // ------------------------------------------------------------ MMA issuer
