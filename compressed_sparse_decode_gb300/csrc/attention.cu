@@ -658,6 +658,7 @@ attention_tc_kernel(const AttParams P) {
                 }
             }
             __syncwarp();
+            const uint64_t part_policy = ptx::l2_policy_evict_first();
             __nv_bfloat16 *dst0 = (P.n_split == 1)
                                       ? P.out + (size_t)r * kHeads * kDim + rank * kHalf
                                       : P.part_o + ((size_t)r * P.n_split + u.split) * kHeads * kDim + rank * kHalf;
@@ -665,7 +666,10 @@ attention_tc_kernel(const AttParams P) {
             for (int i = 0; i < 32; ++i) {
                 const int hr = quarter * 32 + i;  // a head row of this warp
                 const uint4 v = *reinterpret_cast<const uint4 *>(ostage + hr * (kHalf * 2) + ((lane ^ (hr & 7)) << 4));
-                reinterpret_cast<uint4 *>(dst0 + (size_t)hr * kDim)[lane] = v;
+                if (P.n_split == 1)
+                    reinterpret_cast<uint4 *>(dst0 + (size_t)hr * kDim)[lane] = v;
+                else  // split partials are read once, by the combine: evict-first
+                    ptx::stg_v4_policy(reinterpret_cast<uint4 *>(dst0 + (size_t)hr * kDim) + lane, v, part_policy);
             }
             if (rank == 0) {
                 if (P.n_split == 1)
@@ -700,6 +704,7 @@ attention_combine_kernel(const __nv_bfloat16 *__restrict__ part_o, const float2 
     const float2 *ml_row = part_ml + (size_t)r * n_split * kHeads + h;
     const uint4 *o_row = reinterpret_cast<const uint4 *>(part_o + ((size_t)r * n_split * kHeads + h) * kDim) + lane * 2;
     const size_t split_stride = (size_t)kHeads * kDim / 8;  // uint4 per split
+    const uint64_t policy = ptx::l2_policy_evict_first();  // the partials are read once
     // (every split writes its partial row, zeros when it had no candidates,
     // so the rows are loaded without waiting for the (max, sum) pairs)
     float M = sk;
@@ -720,8 +725,8 @@ attention_combine_kernel(const __nv_bfloat16 *__restrict__ part_o, const float2 
             const int sp = s0 + q;
             if (sp < n_split) {
                 ml[q] = ml_row[(size_t)sp * kHeads];
-                v[q][0] = o_row[sp * split_stride];
-                v[q][1] = o_row[sp * split_stride + 1];
+                v[q][0] = ptx::ldg_v4_policy(o_row + sp * split_stride, policy);
+                v[q][1] = ptx::ldg_v4_policy(o_row + sp * split_stride + 1, policy);
             } else {
                 ml[q] = make_float2(0.f, 0.f);
                 v[q][0] = v[q][1] = make_uint4(0, 0, 0, 0);

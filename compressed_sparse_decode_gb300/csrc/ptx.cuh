@@ -313,6 +313,21 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t re
 
 
 // 16-byte global -> shared copy through the load/store path (L1 bypassed).
+// 16-byte global load / store with an L2 cache policy (read-only data for
+// the load).
+__device__ __forceinline__ uint4 ldg_v4_policy(const void *gptr, uint64_t policy) {
+    uint4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(reinterpret_cast<uint64_t>(gptr)), "l"(policy));
+    return v;
+}
+__device__ __forceinline__ void stg_v4_policy(void *gptr, uint4 v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(reinterpret_cast<uint64_t>(gptr)),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
+                 : "memory");
+}
+
 // The same with an L2 cache policy (e.g. l2_policy_evict_first()).
 __device__ __forceinline__ void cp_async_16_hint(void *smem_dst, const void *gsrc, uint64_t policy) {
     asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),

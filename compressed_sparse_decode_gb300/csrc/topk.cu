@@ -111,8 +111,11 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
         int j = 0;
         if ((Ncap & 3) == 0 && (run & 3) == 0) {
             const float4 *r4 = reinterpret_cast<const float4 *>(row + mine);
+            const uint64_t policy = ptx::l2_policy_evict_first();  // the logits are read once
             for (; j + 3 < n_my; j += 4) {
-                const float4 v = __ldg(r4 + (j >> 2));
+                const uint4 w = ptx::ldg_v4_policy(r4 + (j >> 2), policy);
+                const float4 v = make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                                             __uint_as_float(w.w));
                 keys[(j + 0) * kThreads + tid] = order_key(v.x);
                 keys[(j + 1) * kThreads + tid] = order_key(v.y);
                 keys[(j + 2) * kThreads + tid] = order_key(v.z);
