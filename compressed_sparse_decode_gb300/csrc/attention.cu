@@ -508,15 +508,19 @@ attention_tc_kernel(const AttParams P) {
         // (BF16 pairs, lane = head), 128 dims per round trip
         if (u.n_chunks > 0) {
             const uint4 *qg = reinterpret_cast<const uint4 *>(P.q + ((size_t)r * kHeads + h) * kDim);
+            // every byte a decode step reads or writes once is marked
+            // evict-first, so that the next step's indexer finds L2 full of
+            // lines it can replace cheaply (measured on the whole step)
+            const uint64_t q_policy = ptx::l2_policy_evict_first();
 #pragma unroll
             for (int c = 0; c < (kDim - kQTmemDims) / 8; ++c)
-                ptx::cp_async_16(sw128(s.qs + (c >> 3) * kQAtom, h, c & 7), qg + kQTmemDims / 8 + c);
+                ptx::cp_async_16_hint(sw128(s.qs + (c >> 3) * kQAtom, h, c & 7), qg + kQTmemDims / 8 + c, q_policy);
             ptx::cp_async_commit();
 #pragma unroll 1
             for (int pp = 0; pp < kQTmemDims / 128; ++pp) {
                 uint4 w[16];
 #pragma unroll
-                for (int v = 0; v < 16; ++v) w[v] = __ldg(qg + pp * 16 + v);
+                for (int v = 0; v < 16; ++v) w[v] = ptx::ldg_v4_policy(qg + pp * 16 + v, q_policy);
 #pragma unroll
                 for (int hp = 0; hp < 2; ++hp) {
                     uint32_t regs[32];
@@ -758,10 +762,10 @@ attention_combine_kernel(const __nv_bfloat16 *__restrict__ part_o, const float2 
     uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)r * kHeads + h) * kDim) + lane * 2;
 #pragma unroll
     for (int e = 0; e < 2; ++e)
-        dst[e] = make_uint4(bf16x2_bits(acc[8 * e + 0] * inv, acc[8 * e + 1] * inv),
+        ptx::stg_v4_policy(dst + e, make_uint4(bf16x2_bits(acc[8 * e + 0] * inv, acc[8 * e + 1] * inv),
                             bf16x2_bits(acc[8 * e + 2] * inv, acc[8 * e + 3] * inv),
                             bf16x2_bits(acc[8 * e + 4] * inv, acc[8 * e + 5] * inv),
-                            bf16x2_bits(acc[8 * e + 6] * inv, acc[8 * e + 7] * inv));
+                            bf16x2_bits(acc[8 * e + 6] * inv, acc[8 * e + 7] * inv)), policy);
     if (lane == 0) lse[(size_t)r * kHeads + h] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
 }
 

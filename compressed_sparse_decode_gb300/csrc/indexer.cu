@@ -361,7 +361,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 if (c < Ncap) {
 #pragma unroll
                     for (int t = 0; t < T; ++t)
-                        lrow[(size_t)t * Ncap + 128 * hm] = c < nvis[t] ? acc[hm][t] * sk[hm] : -INFINITY;
+                        // streaming store: the logits are read once, by the top-k
+                        __stcs(lrow + (size_t)t * Ncap + 128 * hm, c < nvis[t] ? acc[hm][t] * sk[hm] : -INFINITY);
                 }
             }
         }
