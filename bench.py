@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--workload", default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--report-configs", action="store_true",
+                    help="print a per-kernel table for every workload instead of the benchmark line")
     return ap.parse_args()
 
 
@@ -535,9 +537,88 @@ def run_reference(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def report_configs(args):
+    """Per-kernel times of every workload in synth.WORKLOADS (a markdown table
+    on stdout, not the benchmark's JSON line): events around each call, five
+    warm-up calls, the median of 30 timed calls over rotating input copies.
+    Roofline = max(algorithmic bytes / measured HBM peak, flops / FP8 peak),
+    with the FP8 dense peak taken as twice the measured BF16 one; the
+    attention's BF16 MMAs make the BF16 figure the tighter one for it."""
+    import numpy as np
+    import torch
+
+    import compressed_sparse_decode_gb300 as csd
+    import synth
+    csd.build()
+    csd.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    hbm = peaks["hbm_gbs"] * 1e9
+    fp8 = 2 * peaks["bf16_tflops"] * 1e12
+    print("| workload | kernel | µs (median) | algorithmic MB | Gflop | roofline µs | fraction |")
+    print("|---|---|---|---|---|---|---|")
+    for name, wl in synth.WORKLOADS.items():
+        base = synth.generate(name, seed=0, device=dev)
+        copies = [base] + [base.clone() for _ in range(N_COPIES - 1)]
+        stream = torch.cuda.Stream(device=dev)
+        q_pos = base.q_pos.cpu().numpy()
+        n_comp = base.n_comp.cpu().numpy()
+        nvis = np.minimum(np.minimum(q_pos // wl.m, n_comp[:, None]), wl.ncap)  # [B, T]
+        nswa = np.minimum(q_pos + 1, wl.W)
+        work = {}
+        if wl.kind == "csa":
+            runners = [Runner(csd, x, stream) for x in copies]
+            with torch.cuda.stream(stream):
+                for r in runners:
+                    r.indexer(); r.topk(); r.attention()
+            torch.cuda.synchronize(dev)
+            cnt = runners[0].cnt.cpu().numpy()
+            cands = int(cnt.sum() + nswa.sum())
+            work["indexer"] = (lambda i: runners[i].indexer(), indexer_bytes(base), 16384 * float(nvis.sum()))
+            work["topk"] = (lambda i: runners[i].topk(), 4 * int(nvis.sum()) + 4 * wl.B * wl.T * wl.k, 0.0)
+            work["attention"] = (lambda i: runners[i].attention(), attention_bytes(runners[0].cnt.cpu().numpy(), base),
+                                 262144.0 * cands)
+        else:
+            comps = [csd.cache_desc(x.comp, wl.ncap, x.seq_stride) for x in copies]
+            outs = [(torch.empty_like(x.q), torch.empty((wl.B, wl.T, 128), dtype=torch.float32, device=dev),
+                     csd.workspace(csd.OP_HCA_ATTENTION, wl.B, wl.T, wl.ncap, 0, dev)) for x in copies]
+
+            def hca(i):
+                x, (o, l, w) = copies[i], outs[i]
+                csd.hca_sink_attention_decode(x.q, x.sink, SCALE, comps[i], x.n_comp, x.ring, wl.W, x.q_pos, wl.m,
+                                              out=o, lse=l, ws=w, stream=stream)
+            cands = int(nvis.sum() + nswa.sum())
+            work["hca attention"] = (hca, cands * 592 + wl.B * wl.T * (2 * 128 * 512 * 2 + 128 * 4), 262144.0 * cands)
+        for kern, (fn, nbytes, flops) in work.items():
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(30)]
+            with torch.cuda.stream(stream):
+                for i in range(5):
+                    fn(i % N_COPIES)
+                for i, (a, b) in enumerate(ev):
+                    a.record(stream)
+                    fn(i % N_COPIES)
+                    b.record(stream)
+            torch.cuda.synchronize(dev)
+            us = float(np.median([a.elapsed_time(b) * 1e3 for a, b in ev]))
+            roof = max(nbytes / hbm, flops / fp8) * 1e6
+            print(f"| {name} | {kern} | {us:.2f} | {nbytes / 1e6:.2f} | {flops / 1e9:.2f} | {roof:.2f} | "
+                  f"{roof / us:.2f} |", flush=True)
+        if csd.csa_read_device_error(stream):
+            raise RuntimeError(f"device error word set on {name}")
+        del copies, base, work
+        torch.cuda.empty_cache()
+    print(f"\npeaks: HBM {peaks['hbm_gbs']:.0f} GB/s, BF16 {peaks['bf16_tflops']:.0f} TFLOP/s ({peaks['source']}); "
+          f"FP8 taken as 2x BF16")
+
+
 def main():
     args = parse()
     rank, world, local_rank = dist_env()
+    if args.report_configs:
+        if rank == 0:
+            report_configs(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world, local_rank)
     else:
