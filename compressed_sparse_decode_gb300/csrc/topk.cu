@@ -2,9 +2,10 @@
 // ("DSV4 Audit", section B2; "ROADMAP -- Stage E", section E7: top-k with
 // warp-level reductions and no global lock).
 //
-// One row (query token) per cluster of 8 CTAs; CTA rank c owns the slice
-// [c * slice, (c + 1) * slice) of the row, and thread t of a CTA owns the
-// contiguous run of E = slice / 512 entries starting at t * E (kept in shared
+// One row (query token) per cluster of 8 CTAs of 512 threads (1024 for rows
+// above 64K entries); CTA rank c owns the slice [c * slice, (c + 1) * slice)
+// of the row, and thread t of a CTA owns the contiguous run of
+// E = slice / threads entries starting at t * E (kept in shared
 // memory transposed, keys[j][t], so every access is conflict-free). The CTA
 // loads its slice once as order-preserving 32-bit keys; a radix select then
 // finds the k-th largest key K* in three digit passes (bits 31..21, 20..10,
@@ -25,8 +26,11 @@ namespace csa {
 namespace {
 
 constexpr int kCtas = 8;                 // CTAs per row (a portable cluster)
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
+// Threads per CTA: 512, or 1024 for rows long enough that 512 threads would
+// hold more than kRunSplit entries each (the per-thread loops of the three
+// passes and the compaction are the kernel's serial work).
+constexpr int kMaxThreads = 1024;
+constexpr int kRunSplit = 16;
 constexpr int kBins = 2048;              // 11-bit digits (the last pass uses 10)
 constexpr int kMaxRun = 64;             // entries per thread held in shared memory
 
@@ -36,13 +40,15 @@ struct TopkShared {
     alignas(16) int peer_counts[kCtas][2];
     alignas(16) uint32_t reduced[3][kBins / kCtas];  // this CTA's range of the cluster-wide histogram
     int range_total[3][kCtas];                       // written by every CTA: its range's total
-    int wsum[kWarps];
+    int wsum[kMaxThreads / 32];
     uint32_t digit;
     int remaining;
 };
 
 // Block-wide exclusive prefix sum of a uint32 (modular); every thread must call it.
+template <int kThreads>
 __device__ __forceinline__ uint32_t block_exclusive_sum_u32(uint32_t v, int *wsum, uint32_t &total) {
+    constexpr int kWarps = kThreads / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t incl = v;
 #pragma unroll
@@ -75,6 +81,7 @@ __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
     asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
+template <int kThreads>
 __global__ void __launch_bounds__(kThreads)
 topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict__ q_pos,
                     const int32_t *__restrict__ n_comp, int T, int Ncap, int m, int k, int run, int resident,
@@ -229,15 +236,15 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
         // one scan of (gt << 16 | eq): a CTA holds fewer than 65536 entries,
         // so the low half never carries into the high half
         uint32_t tot_packed;
-        const uint32_t excl = block_exclusive_sum_u32(((uint32_t)gt << 16) | (uint32_t)eq, s.wsum, tot_packed);
+        const uint32_t excl = block_exclusive_sum_u32<kThreads>(((uint32_t)gt << 16) | (uint32_t)eq, s.wsum, tot_packed);
         gt_excl = (int)(excl >> 16);
         eq_excl = (int)(excl & 0xFFFFu);
         tot_gt = (int)(tot_packed >> 16);
         tot_eq = (int)(tot_packed & 0xFFFFu);
     } else {
         uint32_t t0, t1;
-        gt_excl = (int)block_exclusive_sum_u32((uint32_t)gt, s.wsum, t0);
-        eq_excl = (int)block_exclusive_sum_u32((uint32_t)eq, s.wsum, t1);
+        gt_excl = (int)block_exclusive_sum_u32<kThreads>((uint32_t)gt, s.wsum, t0);
+        eq_excl = (int)block_exclusive_sum_u32<kThreads>((uint32_t)eq, s.wsum, t1);
         tot_gt = (int)t0;
         tot_eq = (int)t1;
     }
@@ -277,13 +284,17 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
 
 size_t topk_workspace_bytes(int, int, int, int) { return 0; }
 
-cudaError_t launch_topk(const float *logits, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap,
-                        int m, int k, int32_t *idx_out, int32_t *cnt_out, void *, size_t, cudaStream_t stream) {
+namespace {
+
+template <int kThreads>
+cudaError_t launch_t(const float *logits, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap, int m,
+                     int k, int32_t *idx_out, int32_t *cnt_out, cudaStream_t stream) {
     const int per_cta = (Ncap + kCtas - 1) / kCtas;
     const int run = (per_cta + kThreads - 1) / kThreads;
     const int resident = run <= kMaxRun ? 1 : 0;
     const size_t smem = sizeof(TopkShared) + (resident ? (size_t)run * kThreads * sizeof(uint32_t) : 0);
-    cudaError_t e = set_max_dynamic_smem_once(reinterpret_cast<const void *>(topk_cluster_kernel), (int)smem);
+    cudaError_t e =
+        set_max_dynamic_smem_once(reinterpret_cast<const void *>(topk_cluster_kernel<kThreads>), (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(B * T * kCtas);
@@ -300,10 +311,20 @@ cudaError_t launch_topk(const float *logits, const int32_t *q_pos, const int32_t
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     count_launch();
-    e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, logits, q_pos, n_comp, T, Ncap, m, k, run, resident, idx_out,
-                           cnt_out);
+    e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel<kThreads>, logits, q_pos, n_comp, T, Ncap, m, k, run, resident,
+                           idx_out, cnt_out);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const float *logits, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap,
+                        int m, int k, int32_t *idx_out, int32_t *cnt_out, void *, size_t, cudaStream_t stream) {
+    const int per_cta = (Ncap + kCtas - 1) / kCtas;
+    if ((per_cta + 511) / 512 > kRunSplit)
+        return launch_t<1024>(logits, q_pos, n_comp, B, T, Ncap, m, k, idx_out, cnt_out, stream);
+    return launch_t<512>(logits, q_pos, n_comp, B, T, Ncap, m, k, idx_out, cnt_out, stream);
 }
 
 }  // namespace csa

@@ -113,15 +113,19 @@ def test_paged_cache_matches_contiguous_and_oracle(cuda_lib):
         assert np.array_equal(kv.cpu().numpy()[r][:okc[r]], okv[r][:okc[r]])
 
 
-def test_topk_heavy_ties_and_extremes(cuda_lib):
+# 5000: 512-thread CTAs; 70001 (ragged, scalar loads) and 131076 (16-byte
+# loads): rows long enough for the 1024-thread CTAs
+@pytest.mark.parametrize("ncap", [5000, 70001, 131076])
+def test_topk_heavy_ties_and_extremes(cuda_lib, ncap):
     rng = np.random.default_rng(0)
-    B, T, ncap = 3, 2, 5000
+    B, T = 3, 2
     vals = rng.integers(-5, 6, size=(B, T, ncap)).astype(np.float32)
     vals[0, 0, 100:200] = 1e30
     vals[1, 1, :] = 0.0                       # all equal: lowest indices win
     vals[2, 0, ::7] = -np.float32(np.inf)
     lg = torch.tensor(vals, device="cuda")
-    q_pos = torch.tensor([[20000, 20001], [19996, 19999], [400, 401]], dtype=torch.int32, device="cuda")
+    q_pos = torch.tensor([[4 * ncap, 4 * ncap + 1], [4 * ncap - 4, 4 * ncap - 1], [400, 401]], dtype=torch.int32,
+                         device="cuda")
     n_comp = torch.tensor([ncap, ncap, ncap], dtype=torch.int32, device="cuda")
     for k in (1, 7, 64, 1000, 2048):
         idx, cnt = cuda_lib.csa_topk(lg, q_pos, n_comp, 4, k)
