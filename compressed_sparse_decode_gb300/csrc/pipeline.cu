@@ -12,7 +12,6 @@
 // so the copies of steps i-1 and i+1 overlap step i's kernels. Every wait is
 // on the latest record of an event, made by step i-depth: calls are issued in
 // step order from the host, so no record of a later step can exist yet.
-#include <cstring>
 #include <new>
 
 #include "common.cuh"

@@ -185,7 +185,6 @@ __host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t a_fmt, uint32_t b_f
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-
 // D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16, A read from tensor memory
 // (rows in lanes, 16-bit K elements packed two per 32-bit column).
 __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -227,24 +226,6 @@ __device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr, uint32_t 
     return d;
 }
 
-// ---------------------------------------------------------------- bulk copies
-
-// Register `bytes` more expected transaction bytes on `bar` (no arrival).
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-// Contiguous global -> shared copy through the TMA engine (16-byte aligned,
-// size a multiple of 16), completing transaction bytes on `bar`.
-__device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
 // ---------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -264,55 +245,8 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
     return r;
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
-                 "f"(v.w)
-                 : "memory");
-}
+// ---------------------------------------------------------------- global memory and cp.async
 
-// Arrive on an mbarrier in another CTA of the cluster (release at cluster scope).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait with cluster-scope acquire (for barriers a peer CTA arrives on).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                                  uint64_t limit_ns) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if ((it & 63u) == 63u) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > limit_ns) return false;
-        }
-    }
-}
-
-
-// Asynchronous store of 16 bytes into another CTA's shared memory; completes
-// 16 transaction bytes on the mbarrier at `remote_bar` (same CTA as `addr`).
-__device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t remote_bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-                     addr),
-                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
-                 : "memory");
-}
-
-
-// 16-byte global -> shared copy through the load/store path (L1 bypassed).
 // 16-byte global load / store with an L2 cache policy (read-only data for
 // the load).
 __device__ __forceinline__ uint4 ldg_v4_policy(const void *gptr, uint64_t policy) {
@@ -328,16 +262,11 @@ __device__ __forceinline__ void stg_v4_policy(void *gptr, uint4 v, uint64_t poli
                  : "memory");
 }
 
-// The same with an L2 cache policy (e.g. l2_policy_evict_first()).
+// 16-byte global -> shared copy through the load/store path (L1 bypassed),
+// with an L2 cache policy (e.g. l2_policy_evict_first()).
 __device__ __forceinline__ void cp_async_16_hint(void *smem_dst, const void *gsrc, uint64_t policy) {
     asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
                  "l"(reinterpret_cast<uint64_t>(gsrc)), "l"(policy)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gsrc) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
-                 "l"(reinterpret_cast<uint64_t>(gsrc))
                  : "memory");
 }
 
@@ -358,56 +287,11 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Arrive on `bar` once every cp.async this thread issued so far has landed
-// (the barrier's expected count includes this arrival).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 // 2^x on the special-function unit (flush-to-zero; 2^-inf = 0).
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-
-// Arrive (once) on the mbarrier at the same shared-memory offset in every CTA
-// of `cta_mask` when every MMA issued so far by this thread is done.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
-// Named barrier over `count` threads (id > 0; id 0 is __syncthreads).
-__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-
-// Bulk copy from this CTA's shared memory into another CTA's shared memory of
-// the cluster (dst and bar are shared::cluster addresses, e.g. from mapa),
-// completing `bytes` transaction bytes on the remote barrier. Its completion
-// (and the end of its reads of `src`) is observable only through that barrier.
-__device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst_cluster, const void *src, uint32_t bytes,
-                                                 uint32_t bar_cluster) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            dst_cluster),
-        "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
-        : "memory");
-}
-
-// 16-byte read-only global load that does not allocate in L1.
-__device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
 }
 
 }  // namespace ptx
