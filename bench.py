@@ -55,6 +55,22 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(values, device, world: int) -> list[float]:
+    """Element-wise maximum of per-rank timings over all ranks (the slowest
+    rank sets the whole job's time); identity on one rank."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput(units_per_rank: int, world: int, ms: float) -> float:
+    """Units of all ranks per second of the slowest rank (weak scaling)."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 # --------------------------------------------------------------------------
 # clocks during the timed region
 # --------------------------------------------------------------------------
@@ -312,15 +328,11 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     t_topk = [b.elapsed_time(c) for _, b, c, _ in bev]
     t_att = [c.elapsed_time(d) for _, _, c, d in bev]
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    (total_ms,) = max_over_ranks([total_ms], dev, world)
     if csd.csa_read_device_error(stream):
         raise RuntimeError("device error word set during the timed region")
 
-    tokens = wl.B * wl.T * args.steps * world
-    value = tokens / (total_ms / 1e3)
+    value = job_throughput(wl.B * wl.T * args.steps, world, total_ms)
     peaks = load_peaks()
     idx_bytes = indexer_bytes(base)
     att_bytes = attention_bytes(runners[0].cnt.cpu().numpy(), base)
@@ -433,16 +445,13 @@ def run_e2e(args, csd, copies, runners, stream, dev, world):
     timed(serial, max(args.warmup, 3))
     ms_serial = timed(serial, args.steps)
     pl.close()
-    if world > 1:
-        tt = torch.tensor([ms, ms_serial], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms, ms_serial = (float(v) for v in tt.tolist())
-    tok = wl.B * wl.T * args.steps * world
-    return {"value": round(tok / (ms / 1e3), 1), "unit": UNIT,
+    ms, ms_serial = max_over_ranks([ms, ms_serial], dev, world)
+    tok = wl.B * wl.T * args.steps
+    return {"value": round(job_throughput(tok, world, ms), 1), "unit": UNIT,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(ms / args.steps, 5),
             "call": "csa_decode_step_host (host inputs and outputs; copies overlap neighbouring steps' kernels)",
             "clock": "host wall clock, synchronised start to csa_pipeline_sync",
-            "serialized": {"value": round(tok / (ms_serial / 1e3), 1),
+            "serialized": {"value": round(job_throughput(tok, world, ms_serial), 1),
                            "ms_per_step": round(ms_serial / args.steps, 5),
                            "call": "torch H2D copies, csa_decode_step, torch D2H copies, one stream"}}
 
