@@ -546,7 +546,7 @@ def run_reference(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
-def report_configs(args):
+def report_configs():
     """Per-kernel times of every workload in synth.WORKLOADS (a markdown table
     on stdout, not the benchmark's JSON line): events around each call, five
     warm-up calls, the median of 30 timed calls over rotating input copies.
@@ -626,7 +626,7 @@ def main():
     rank, world, local_rank = dist_env()
     if args.report_configs:
         if rank == 0:
-            report_configs(args)
+            report_configs()
         return
     if args.impl == "reference":
         run_reference(args, rank, world, local_rank)
