@@ -199,17 +199,18 @@ class Runner:
                                    x.page_records if x.block_table is not None else 0)
         s = C.c_void_p(stream.cuda_stream)
         p = lambda t: C.c_void_p(t.data_ptr()) if t is not None else None
+        st = p(csd.status_word(dev))
         nb = lambda t: C.c_size_t(0 if t is None else t.numel())
         R = x.ring.shape[1]
         self.a_idx = [p(x.q_idx), p(x.q_idx_scale), p(x.w_idx), p(x.k_idx), p(x.k_idx_scale), p(x.q_pos),
-                      p(x.n_comp), B, T, N, wl.m, p(self.logits), s]
+                      p(x.n_comp), B, T, N, wl.m, p(self.logits), st, s]
         self.a_topk = [p(self.logits), p(x.q_pos), p(x.n_comp), B, T, N, wl.m, k, p(self.idx), p(self.cnt),
-                       p(self.ws_topk), nb(self.ws_topk), s]
+                       p(self.ws_topk), nb(self.ws_topk), st, s]
         self.a_att = [p(x.q), p(x.sink), C.c_float(SCALE), self.comp, p(x.ring), R, wl.W, p(self.idx), p(self.cnt),
-                      p(x.q_pos), B, T, k, p(self.out), p(self.lse), p(self.ws_att), nb(self.ws_att), s]
+                      p(x.q_pos), B, T, k, p(self.out), p(self.lse), p(self.ws_att), nb(self.ws_att), st, s]
         self.a_step = [p(x.q_idx), p(x.q_idx_scale), p(x.w_idx), p(x.k_idx), p(x.k_idx_scale), p(x.q), p(x.sink),
                        C.c_float(SCALE), self.comp, p(x.ring), R, wl.W, p(x.q_pos), p(x.n_comp), B, T, N, wl.m, k,
-                       p(self.out), p(self.lse), None, None, p(self.ws_step), nb(self.ws_step), s]
+                       p(self.out), p(self.lse), None, None, p(self.ws_step), nb(self.ws_step), st, s]
 
     def indexer(self):
         st = self.lib.csa_indexer_logits(*self.a_idx)
@@ -408,7 +409,7 @@ def run_e2e(args, csd, copies, runners, stream, dev, world):
         step_args.append([C.c_void_p(pl.handle), p(hi[0]), p(hi[1]), p(hi[2]), p(hi[3]), p(hi[4]), p(x.k_idx),
                           p(x.k_idx_scale), p(x.sink), C.c_float(SCALE), r.comp, p(x.ring), x.ring.shape[1], wl.W,
                           p(x.n_comp), wl.ncap, wl.m, wl.k, p(ho), p(hl), p(r.ws_step), C.c_size_t(r.ws_step.numel()),
-                          None])
+                          p(csd.status_word(dev)), None])
 
     def pipelined(n):
         for i in range(n):

@@ -28,7 +28,8 @@ OP_INDEXER, OP_TOPK, OP_ATTENTION, OP_HCA_ATTENTION, OP_DECODE_STEP = range(5)
 
 EXPORTED = ["csa_workspace_bytes", "csa_indexer_logits", "csa_topk", "csa_gather_swa",
             "csa_sink_attention_decode", "hca_sink_attention_decode", "csa_decode_step",
-            "csa_read_device_error", "csa_status_string", "csa_version", "csa_kernel_launches",
+            "csa_check_device_status", "csa_read_device_error", "csa_debug_set_wait_limit_ns",
+            "csa_status_string", "csa_version", "csa_kernel_launches",
             "csa_sink_attention_decode_noalloc", "csa_pipeline_staging_bytes", "csa_pipeline_create",
             "csa_decode_step_host", "csa_pipeline_wait", "csa_pipeline_sync", "csa_pipeline_destroy"]
 PIPELINE_MAX_DEPTH = 4
@@ -68,30 +69,30 @@ def load(path: str | None = None):
         lib.csa_status_string.restype = C.c_char_p
         lib.csa_workspace_bytes.argtypes = [C.c_int, i32, i32, i32, i32]
         lib.csa_workspace_bytes.restype = sz
-        lib.csa_indexer_logits.argtypes = [P] * 7 + [i32] * 4 + [P, P]
+        lib.csa_indexer_logits.argtypes = [P] * 7 + [i32] * 4 + [P, P, P]
         lib.csa_indexer_logits.restype = st
-        lib.csa_topk.argtypes = [P, P, P] + [i32] * 5 + [P, P, P, sz, P]
+        lib.csa_topk.argtypes = [P, P, P] + [i32] * 5 + [P, P, P, sz, P, P]
         lib.csa_topk.restype = st
-        lib.csa_gather_swa.argtypes = [csa_cache_desc, P, i32, i32, P, P, P, i32, i32, i32, P, P, P]
+        lib.csa_gather_swa.argtypes = [csa_cache_desc, P, i32, i32, P, P, P, i32, i32, i32, P, P, P, P]
         lib.csa_gather_swa.restype = st
         lib.csa_sink_attention_decode.argtypes = ([P, P, f32, csa_cache_desc, P, i32, i32, P, P, P, i32, i32, i32,
-                                                   P, P, P, sz, P])
+                                                   P, P, P, sz, P, P])
         lib.csa_sink_attention_decode.restype = st
         lib.hca_sink_attention_decode.argtypes = ([P, P, f32, csa_cache_desc, P, P, i32, i32, P, i32, i32, i32,
-                                                   P, P, P, sz, P])
+                                                   P, P, P, sz, P, P])
         lib.hca_sink_attention_decode.restype = st
         lib.csa_decode_step.argtypes = ([P] * 7 + [f32, csa_cache_desc, P, i32, i32, P, P] + [i32] * 5
-                                        + [P, P, P, P, P, sz, P])
+                                        + [P, P, P, P, P, sz, P, P])
         lib.csa_decode_step.restype = st
         lib.csa_sink_attention_decode_noalloc.argtypes = ([P, P, f32, csa_cache_desc, P, i32, i32, P, P, P, i32, i32,
-                                                           i32, P, P, P])
+                                                           i32, P, P, P, P])
         lib.csa_sink_attention_decode_noalloc.restype = st
         lib.csa_pipeline_staging_bytes.argtypes = [i32, i32, i32]
         lib.csa_pipeline_staging_bytes.restype = sz
         lib.csa_pipeline_create.argtypes = [C.POINTER(C.c_void_p), i32, i32, i32, P, sz, P]
         lib.csa_pipeline_create.restype = st
         lib.csa_decode_step_host.argtypes = ([P] * 9 + [f32, csa_cache_desc, P, i32, i32, P] + [i32] * 3
-                                             + [P, P, P, sz, C.POINTER(C.c_int64)])
+                                             + [P, P, P, sz, P, C.POINTER(C.c_int64)])
         lib.csa_decode_step_host.restype = st
         lib.csa_pipeline_wait.argtypes = [P, C.c_int64]
         lib.csa_pipeline_wait.restype = st
@@ -99,8 +100,12 @@ def load(path: str | None = None):
         lib.csa_pipeline_sync.restype = st
         lib.csa_pipeline_destroy.argtypes = [P]
         lib.csa_pipeline_destroy.restype = st
-        lib.csa_read_device_error.argtypes = [C.POINTER(C.c_int32), P]
+        lib.csa_check_device_status.argtypes = [P, P, P]
+        lib.csa_check_device_status.restype = st
+        lib.csa_read_device_error.argtypes = [P, C.POINTER(C.c_int32), P]
         lib.csa_read_device_error.restype = st
+        lib.csa_debug_set_wait_limit_ns.argtypes = [C.c_uint64]
+        lib.csa_debug_set_wait_limit_ns.restype = None
         _lib = lib
         return lib
 
@@ -143,6 +148,30 @@ def _ptr(t: torch.Tensor | None, name: str, dtype=None, shape=None):
     return t.data_ptr()
 
 
+_status_words: dict[int, torch.Tensor] = {}
+
+
+def status_word(device=None) -> torch.Tensor:
+    """The binding's default status word for a device: one int32 in device
+    memory (created zeroed on first use), passed to the library by every call
+    below that is not given its own ``status`` tensor."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    with _lock:
+        w = _status_words.get(dev.index)
+        if w is None:
+            w = torch.zeros(1, dtype=torch.int32, device=dev)
+            _status_words[dev.index] = w
+    return w
+
+
+def _status(status, device) -> int:
+    if status is None:
+        status = status_word(device)
+    return _ptr(status, "status", torch.int32, (1,))
+
+
 def cache_desc(records: torch.Tensor, seq_capacity: int, seq_stride: int = 0,
                block_table: torch.Tensor | None = None, page_records: int = 0) -> csa_cache_desc:
     """Describe a cache of latent records: ``records`` is uint8 [n, 592] (or
@@ -179,7 +208,7 @@ def workspace(op: int, B: int, T: int, Ncap: int, k: int, device=None) -> torch.
 
 
 def csa_indexer_logits(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q_pos, n_comp, m: int,
-                       logits: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                       logits: torch.Tensor | None = None, stream=None, status=None) -> torch.Tensor:
     B, T = q_pos.shape
     Ncap = k_idx.shape[1]
     if logits is None:
@@ -192,12 +221,14 @@ def csa_indexer_logits(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q_pos, n_c
             _ptr(k_idx_scale, "k_idx_scale", torch.float32, (B, Ncap)),
             _ptr(q_pos, "q_pos", torch.int32, (B, T)), _ptr(n_comp, "n_comp", torch.int32, (B,))]
     _check(load().csa_indexer_logits(*args, B, T, Ncap, int(m),
-                                     _ptr(logits, "logits", torch.float32, (B, T, Ncap)), _stream(stream)),
+                                     _ptr(logits, "logits", torch.float32, (B, T, Ncap)),
+                                     _status(status, q_idx.device), _stream(stream)),
            "csa_indexer_logits")
     return logits
 
 
-def csa_topk(logits, q_pos, n_comp, m: int, k: int, topk_idx=None, topk_cnt=None, ws=None, stream=None):
+def csa_topk(logits, q_pos, n_comp, m: int, k: int, topk_idx=None, topk_cnt=None, ws=None, stream=None,
+             status=None):
     B, T, Ncap = logits.shape
     dev = logits.device
     if topk_idx is None:
@@ -210,13 +241,14 @@ def csa_topk(logits, q_pos, n_comp, m: int, k: int, topk_idx=None, topk_cnt=None
                            _ptr(n_comp, "n_comp", torch.int32, (B,)), B, T, Ncap, int(m), int(k),
                            _ptr(topk_idx, "topk_idx", torch.int32, (B, T, k)),
                            _ptr(topk_cnt, "topk_cnt", torch.int32, (B, T)),
-                           _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _stream(stream)),
+                           _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(),
+                           _status(status, dev), _stream(stream)),
            "csa_topk")
     return topk_idx, topk_cnt
 
 
 def csa_gather_swa(comp: csa_cache_desc, swa_ring, W: int, topk_idx, topk_cnt, q_pos, kv_out=None, kv_cnt=None,
-                   stream=None):
+                   stream=None, status=None):
     B, T, k = topk_idx.shape
     R = swa_ring.shape[1]
     dev = swa_ring.device
@@ -228,12 +260,13 @@ def csa_gather_swa(comp: csa_cache_desc, swa_ring, W: int, topk_idx, topk_cnt, q
                                  _ptr(topk_idx, "topk_idx", torch.int32), _ptr(topk_cnt, "topk_cnt", torch.int32, (B, T)),
                                  _ptr(q_pos, "q_pos", torch.int32, (B, T)), B, T, k,
                                  _ptr(kv_out, "kv_out", torch.uint8, (B, T, k + W, RECORD_BYTES)),
-                                 _ptr(kv_cnt, "kv_cnt", torch.int32, (B, T)), _stream(stream)), "csa_gather_swa")
+                                 _ptr(kv_cnt, "kv_cnt", torch.int32, (B, T)), _status(status, dev), _stream(stream)),
+           "csa_gather_swa")
     return kv_out, kv_cnt
 
 
 def csa_sink_attention_decode(q, sink, softmax_scale: float, comp: csa_cache_desc, swa_ring, W: int, topk_idx,
-                              topk_cnt, q_pos, out=None, lse=None, ws=None, stream=None):
+                              topk_cnt, q_pos, out=None, lse=None, ws=None, stream=None, status=None):
     B, T = q_pos.shape
     k = topk_idx.shape[2]
     R = swa_ring.shape[1]
@@ -250,13 +283,13 @@ def csa_sink_attention_decode(q, sink, softmax_scale: float, comp: csa_cache_des
         _ptr(topk_idx, "topk_idx", torch.int32, (B, T, k)), _ptr(topk_cnt, "topk_cnt", torch.int32, (B, T)),
         _ptr(q_pos, "q_pos", torch.int32, (B, T)), B, T, k,
         _ptr(out, "out", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(lse, "lse", torch.float32, (B, T, HEADS)),
-        _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _stream(stream)),
+        _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _status(status, dev), _stream(stream)),
         "csa_sink_attention_decode")
     return out, lse
 
 
 def csa_sink_attention_decode_noalloc(q, sink, softmax_scale: float, comp: csa_cache_desc, swa_ring, W: int, topk_idx,
-                                      topk_cnt, q_pos, out=None, lse=None, stream=None):
+                                      topk_cnt, q_pos, out=None, lse=None, stream=None, status=None):
     """csa_sink_attention_decode without a workspace: for callers that cannot
     allocate device memory on the decode path (see include/csa.h); the split
     partials use the library's static device scratch."""
@@ -274,12 +307,12 @@ def csa_sink_attention_decode_noalloc(q, sink, softmax_scale: float, comp: csa_c
         _ptr(topk_idx, "topk_idx", torch.int32, (B, T, k)), _ptr(topk_cnt, "topk_cnt", torch.int32, (B, T)),
         _ptr(q_pos, "q_pos", torch.int32, (B, T)), B, T, k,
         _ptr(out, "out", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(lse, "lse", torch.float32, (B, T, HEADS)),
-        _stream(stream)), "csa_sink_attention_decode_noalloc")
+        _status(status, dev), _stream(stream)), "csa_sink_attention_decode_noalloc")
     return out, lse
 
 
 def hca_sink_attention_decode(q, sink, softmax_scale: float, comp: csa_cache_desc, n_comp, swa_ring, W: int, q_pos,
-                              m_hca: int = 128, out=None, lse=None, ws=None, stream=None):
+                              m_hca: int = 128, out=None, lse=None, ws=None, stream=None, status=None):
     B, T = q_pos.shape
     R = swa_ring.shape[1]
     dev = q.device
@@ -295,14 +328,14 @@ def hca_sink_attention_decode(q, sink, softmax_scale: float, comp: csa_cache_des
         _ptr(swa_ring, "swa_ring", torch.uint8, (B, R, RECORD_BYTES)), R, int(W),
         _ptr(q_pos, "q_pos", torch.int32, (B, T)), B, T, int(m_hca),
         _ptr(out, "out", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(lse, "lse", torch.float32, (B, T, HEADS)),
-        _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _stream(stream)),
+        _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _status(status, dev), _stream(stream)),
         "hca_sink_attention_decode")
     return out, lse
 
 
 def csa_decode_step(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q, sink, softmax_scale: float,
                     comp: csa_cache_desc, swa_ring, W: int, q_pos, n_comp, m: int, k: int, out=None, lse=None,
-                    topk_idx=None, topk_cnt=None, ws=None, stream=None):
+                    topk_idx=None, topk_cnt=None, ws=None, stream=None, status=None):
     B, T = q_pos.shape
     Ncap = k_idx.shape[1]
     R = swa_ring.shape[1]
@@ -325,7 +358,8 @@ def csa_decode_step(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q, sink, soft
         B, T, Ncap, int(m), int(k),
         _ptr(out, "out", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(lse, "lse", torch.float32, (B, T, HEADS)),
         _ptr(topk_idx, "topk_idx", torch.int32, (B, T, k)), _ptr(topk_cnt, "topk_cnt", torch.int32, (B, T)),
-        _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _stream(stream)), "csa_decode_step")
+        _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _status(status, dev), _stream(stream)),
+        "csa_decode_step")
     return out, lse
 
 
@@ -357,7 +391,7 @@ def csa_pipeline_create(B: int, T: int, depth: int, staging: torch.Tensor, strea
 
 def csa_decode_step_host(pipeline: int, B: int, T: int, h_q_idx, h_q_idx_scale, h_w_idx, h_q, h_q_pos, k_idx,
                          k_idx_scale, sink, softmax_scale: float, comp: csa_cache_desc, swa_ring, W: int, n_comp,
-                         m: int, k: int, h_out, h_lse, ws) -> int:
+                         m: int, k: int, h_out, h_lse, ws, status=None) -> int:
     """Enqueue one step; h_* are host tensors (page-locked for overlap), the
     rest is the device-resident layer state. Returns the step's ordinal."""
     Ncap = k_idx.shape[1]
@@ -374,7 +408,8 @@ def csa_decode_step_host(pipeline: int, B: int, T: int, h_q_idx, h_q_idx_scale, 
         _ptr(swa_ring, "swa_ring", torch.uint8, (B, R, RECORD_BYTES)), R, int(W),
         _ptr(n_comp, "n_comp", torch.int32, (B,)), Ncap, int(m), int(k),
         _hptr(h_out, "h_out", torch.bfloat16, (B, T, HEADS, DIM)), _hptr(h_lse, "h_lse", torch.float32, (B, T, HEADS)),
-        _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), C.byref(step)), "csa_decode_step_host")
+        _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _status(status, k_idx.device),
+        C.byref(step)), "csa_decode_step_host")
     return int(step.value)
 
 
@@ -404,10 +439,10 @@ class HostPipeline:
         self.handle = csa_pipeline_create(B, T, depth, self.staging, stream)
 
     def step(self, h_q_idx, h_q_idx_scale, h_w_idx, h_q, h_q_pos, k_idx, k_idx_scale, sink, softmax_scale, comp,
-             swa_ring, W, n_comp, m, k, h_out, h_lse, ws) -> int:
+             swa_ring, W, n_comp, m, k, h_out, h_lse, ws, status=None) -> int:
         return csa_decode_step_host(self.handle, self.B, self.T, h_q_idx, h_q_idx_scale, h_w_idx, h_q, h_q_pos,
                                     k_idx, k_idx_scale, sink, softmax_scale, comp, swa_ring, W, n_comp, m, k,
-                                    h_out, h_lse, ws)
+                                    h_out, h_lse, ws, status)
 
     def wait(self, step: int):
         csa_pipeline_wait(self.handle, step)
@@ -427,8 +462,29 @@ class HostPipeline:
             pass
 
 
-def csa_read_device_error(stream=None) -> int:
-    """Read and clear the device error word (synchronises the stream)."""
+def csa_check_device_status(host_status: torch.Tensor, status: torch.Tensor | None = None, stream=None,
+                            device=None):
+    """Enqueue (no synchronisation) a copy of the status word into
+    ``host_status`` (an int32 CPU tensor of one element, page-locked for an
+    asynchronous copy) and a reset of the word. Read ``host_status`` once the
+    stream has passed this point."""
+    if host_status.is_cuda or host_status.dtype != torch.int32 or host_status.numel() != 1:
+        raise ValueError("host_status must be a one-element int32 CPU tensor")
+    dev = status.device if status is not None else device
+    _check(load().csa_check_device_status(_status(status, dev), host_status.data_ptr(), _stream(stream)),
+           "csa_check_device_status")
+
+
+def csa_read_device_error(stream=None, status: torch.Tensor | None = None, device=None) -> int:
+    """Read and clear a status word (the device's default one unless given);
+    blocking: synchronises the stream. For tests and diagnostics."""
     code = C.c_int32(0)
-    _check(load().csa_read_device_error(C.byref(code), _stream(stream)), "csa_read_device_error")
+    dev = status.device if status is not None else device
+    _check(load().csa_read_device_error(_status(status, dev), C.byref(code), _stream(stream)), "csa_read_device_error")
     return int(code.value)
+
+
+def csa_debug_set_wait_limit_ns(ns: int):
+    """Diagnostic: limit of the kernels' bounded waits for later launches (0 =
+    the default of one second); see include/csa.h."""
+    load().csa_debug_set_wait_limit_ns(int(ns))

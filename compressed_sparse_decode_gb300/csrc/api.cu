@@ -1,6 +1,8 @@
 // api.cu -- the extern "C" entry points of libcsa: host-side argument checks,
 // workspace carving and kernel launches. No call allocates device memory or
 // synchronises the device (except csa_read_device_error, a diagnostic).
+// In-kernel problems go to the caller's status word (an int32 in device
+// memory passed to every compute call).
 #include <cstdint>
 #include <atomic>
 #include <cstring>
@@ -16,10 +18,10 @@ cudaError_t launch_topk(const float *, const int32_t *, const int32_t *, int, in
                         int32_t *, void *, size_t, cudaStream_t);
 cudaError_t launch_gather(const csa_cache_desc &, const void *, int, int, const int32_t *, const int32_t *,
                           const int32_t *, int, int, int, void *, int32_t *, int *, cudaStream_t);
-size_t attention_workspace_bytes(int, int, int);
+size_t attention_workspace_bytes(int B, int T, int max_selected, int W);
 cudaError_t launch_attention(const void *, const float *, float, const csa_cache_desc &, const void *, int, int,
                              const int32_t *, const int32_t *, const int32_t *, int, const int32_t *, int, int, int,
-                             bool, int, void *, float *, void *, size_t, int *, cudaStream_t);
+                             bool, void *, float *, void *, size_t, int *, cudaStream_t);
 }  // namespace csa
 
 namespace csa {
@@ -37,6 +39,15 @@ SmemOptIn g_smem_opt_in[64];
 int g_n_smem_opt_in;
 std::mutex g_host_cache_mu;
 }  // namespace
+
+namespace {
+std::atomic<uint64_t> g_wait_limit_ns{0};
+}
+void set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns, std::memory_order_relaxed); }
+uint64_t wait_limit_ns() {
+    const uint64_t v = g_wait_limit_ns.load(std::memory_order_relaxed);
+    return v ? v : kDefaultWaitNs;
+}
 
 int cached_sm_count() {
     int dev = 0;
@@ -68,26 +79,6 @@ using namespace csa;
 
 namespace {
 
-// One sticky error word per device, written by kernels (first error wins).
-__device__ int g_device_error;
-
-constexpr int kMaxDevices = 64;
-int *g_err_ptr[kMaxDevices];
-std::mutex g_err_mu;
-
-// Device address of this device's error word; looked up once per device.
-int *device_error_word() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> g(g_err_mu);
-    if (!g_err_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-        g_err_ptr[dev] = static_cast<int *>(p);
-    }
-    return g_err_ptr[dev];
-}
-
 constexpr size_t kWsAlign = 256;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -96,6 +87,11 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 csa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
 
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+}  // namespace
+
+namespace csa {
 bool valid_cache(const csa_cache_desc &c, int B) {
     if (!c.base || !aligned16(c.base) || c.n_records <= 0 || c.seq_capacity <= 0) return false;
     if (c.block_table) {
@@ -109,11 +105,21 @@ bool valid_cache(const csa_cache_desc &c, int B) {
 
 bool valid_dims(int B, int T) { return B >= 1 && T >= 1 && T <= CSA_MAX_TOKENS_PER_SEQ && (int64_t)B * T <= 65535; }
 
-}  // namespace
+bool valid_status_word(const int32_t *status) { return aligned4(status); }
 
-namespace csa {
-// Error word of the current device, for entry points defined in other files.
-int *error_word_for_current_device() { return device_error_word(); }
+csa_status_t attention_arg_status(const void *q, const float *sink, float softmax_scale, const csa_cache_desc &comp,
+                                  const void *swa_ring, int R, int W, const int32_t *topk_idx,
+                                  const int32_t *topk_cnt, const int32_t *q_pos, int B, int T, int k,
+                                  const void *out, const float *lse, const int32_t *status) {
+    if (!q || !sink || !swa_ring || !topk_idx || !topk_cnt || !q_pos || !out || !lse) return CSA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(swa_ring) || !aligned16(out) || !valid_cache(comp, B) ||
+        !valid_status_word(status))
+        return CSA_ERR_INVALID_ARG;
+    if (!valid_dims(B, T) || k < 1 || W < 1 || W > CSA_MAX_SWA_WINDOW || R < W || !(softmax_scale > 0.f))
+        return CSA_ERR_INVALID_ARG;
+    if (k > CSA_MAX_TOPK) return CSA_ERR_UNSUPPORTED;
+    return CSA_OK;
+}
 
 // The host-side checks of csa_indexer_logits, csa_topk and
 // csa_sink_attention_decode for the arguments csa_decode_step passes them, so
@@ -123,8 +129,9 @@ csa_status_t decode_step_arg_status(const uint8_t *q_idx, const float *q_idx_sca
                                     float softmax_scale, const csa_cache_desc &comp, const void *swa_ring, int R,
                                     int W, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap,
                                     int m, int k, const void *out, const float *lse, const int32_t *topk_idx,
-                                    const void *workspace, size_t workspace_bytes) {
+                                    const void *workspace, size_t workspace_bytes, const int32_t *status) {
     if (!valid_dims(B, T) || Ncap < 1 || k < 1 || m < 1) return CSA_ERR_INVALID_ARG;
+    if (!valid_status_word(status)) return CSA_ERR_INVALID_ARG;
     if (!q_idx || !q_idx_scale || !w_idx || !k_idx || !k_idx_scale || !q || !sink || !swa_ring || !q_pos ||
         !n_comp || !out || !lse)
         return CSA_ERR_INVALID_ARG;
@@ -166,13 +173,13 @@ size_t csa_workspace_bytes(csa_op_t op, int B, int T, int Ncap, int k) {
     switch (op) {
     case CSA_OP_INDEXER: return 0;
     case CSA_OP_TOPK: return topk_workspace_bytes(B, T, Ncap, k);
-    case CSA_OP_ATTENTION: return attention_workspace_bytes(B, T, k + CSA_MAX_SWA_WINDOW);
-    case CSA_OP_HCA_ATTENTION: return attention_workspace_bytes(B, T, Ncap + CSA_MAX_SWA_WINDOW);
+    case CSA_OP_ATTENTION: return attention_workspace_bytes(B, T, k, CSA_MAX_SWA_WINDOW);
+    case CSA_OP_HCA_ATTENTION: return attention_workspace_bytes(B, T, Ncap, CSA_MAX_SWA_WINDOW);
     case CSA_OP_DECODE_STEP:
         return align_up(sizeof(float) * (size_t)B * T * Ncap, kWsAlign) +
                2 * align_up(sizeof(int32_t) * (size_t)B * T * k, kWsAlign) +
                align_up(topk_workspace_bytes(B, T, Ncap, k), kWsAlign) +
-               align_up(attention_workspace_bytes(B, T, k + CSA_MAX_SWA_WINDOW), kWsAlign);
+               align_up(attention_workspace_bytes(B, T, k, CSA_MAX_SWA_WINDOW), kWsAlign);
     }
     return 0;
 }
@@ -180,23 +187,23 @@ size_t csa_workspace_bytes(csa_op_t op, int B, int T, int Ncap, int k) {
 csa_status_t csa_indexer_logits(const uint8_t *q_idx, const float *q_idx_scale, const float *w_idx,
                                 const uint8_t *k_idx, const float *k_idx_scale, const int32_t *q_pos,
                                 const int32_t *n_comp, int B, int T, int Ncap, int m, float *logits,
-                                cudaStream_t stream) {
+                                int32_t *status, cudaStream_t stream) {
     if (!q_idx || !q_idx_scale || !w_idx || !k_idx || !k_idx_scale || !q_pos || !n_comp || !logits)
         return CSA_ERR_INVALID_ARG;
     if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(logits) || !aligned16(q_idx_scale) ||
-        !aligned16(w_idx) || !aligned16(k_idx_scale))
+        !aligned16(w_idx) || !aligned16(k_idx_scale) || !valid_status_word(status))
         return CSA_ERR_INVALID_ARG;
     if (!valid_dims(B, T) || Ncap < 1 || m < 1) return CSA_ERR_INVALID_ARG;
     if ((int64_t)B * Ncap >= ((int64_t)1 << 31)) return CSA_ERR_UNSUPPORTED;
     return cuda_status(launch_indexer(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q_pos, n_comp, B, T, Ncap, m,
-                                      logits, device_error_word(), stream));
+                                      logits, status, stream));
 }
 
 csa_status_t csa_topk(const float *logits, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap,
                       int m, int k, int32_t *topk_idx, int32_t *topk_cnt, void *workspace, size_t workspace_bytes,
-                      cudaStream_t stream) {
+                      int32_t *status, cudaStream_t stream) {
     if (!logits || !q_pos || !n_comp || !topk_idx || !topk_cnt) return CSA_ERR_INVALID_ARG;
-    if (!aligned16(logits) || !aligned16(topk_idx)) return CSA_ERR_INVALID_ARG;
+    if (!aligned16(logits) || !aligned16(topk_idx) || !valid_status_word(status)) return CSA_ERR_INVALID_ARG;
     if (!valid_dims(B, T) || Ncap < 1 || m < 1 || k < 1) return CSA_ERR_INVALID_ARG;
     if (k > Ncap || k > CSA_MAX_TOPK) return CSA_ERR_UNSUPPORTED;
     const size_t need = topk_workspace_bytes(B, T, Ncap, k);
@@ -208,45 +215,47 @@ csa_status_t csa_topk(const float *logits, const int32_t *q_pos, const int32_t *
 
 csa_status_t csa_gather_swa(csa_cache_desc comp, const void *swa_ring, int R, int W, const int32_t *topk_idx,
                             const int32_t *topk_cnt, const int32_t *q_pos, int B, int T, int k, void *kv_out,
-                            int32_t *kv_cnt, cudaStream_t stream) {
+                            int32_t *kv_cnt, int32_t *status, cudaStream_t stream) {
     if (!swa_ring || !topk_idx || !topk_cnt || !q_pos || !kv_out || !kv_cnt) return CSA_ERR_INVALID_ARG;
-    if (!aligned16(swa_ring) || !aligned16(kv_out) || !valid_cache(comp, B)) return CSA_ERR_INVALID_ARG;
+    if (!aligned16(swa_ring) || !aligned16(kv_out) || !valid_cache(comp, B) || !valid_status_word(status))
+        return CSA_ERR_INVALID_ARG;
     if (!valid_dims(B, T) || k < 1 || W < 1 || W > CSA_MAX_SWA_WINDOW || R < W) return CSA_ERR_INVALID_ARG;
     return cuda_status(launch_gather(comp, swa_ring, R, W, topk_idx, topk_cnt, q_pos, B, T, k, kv_out, kv_cnt,
-                                     device_error_word(), stream));
+                                     status, stream));
 }
 
 csa_status_t csa_sink_attention_decode(const void *q, const float *sink, float softmax_scale, csa_cache_desc comp,
                                        const void *swa_ring, int R, int W, const int32_t *topk_idx,
                                        const int32_t *topk_cnt, const int32_t *q_pos, int B, int T, int k, void *out,
-                                       float *lse, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
-    if (!q || !sink || !swa_ring || !topk_idx || !topk_cnt || !q_pos || !out || !lse) return CSA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(swa_ring) || !aligned16(out) || !valid_cache(comp, B)) return CSA_ERR_INVALID_ARG;
-    if (!valid_dims(B, T) || k < 1 || W < 1 || W > CSA_MAX_SWA_WINDOW || R < W || !(softmax_scale > 0.f))
-        return CSA_ERR_INVALID_ARG;
-    if (k > CSA_MAX_TOPK) return CSA_ERR_UNSUPPORTED;
-    const size_t need = attention_workspace_bytes(B, T, k + CSA_MAX_SWA_WINDOW);
+                                       float *lse, void *workspace, size_t workspace_bytes, int32_t *status,
+                                       cudaStream_t stream) {
+    const csa_status_t a = attention_arg_status(q, sink, softmax_scale, comp, swa_ring, R, W, topk_idx, topk_cnt,
+                                                q_pos, B, T, k, out, lse, status);
+    if (a != CSA_OK) return a;
+    const size_t need = attention_workspace_bytes(B, T, k, W);
     if (need && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign)))
         return CSA_ERR_WORKSPACE;
     return cuda_status(launch_attention(q, sink, softmax_scale, comp, swa_ring, R, W, topk_idx, topk_cnt, nullptr, 1,
-                                        q_pos, B, T, k, false, k + CSA_MAX_SWA_WINDOW, out, lse, workspace,
-                                        workspace_bytes, device_error_word(), stream));
+                                        q_pos, B, T, k, false, out, lse, workspace, workspace_bytes, status, stream));
 }
 
 csa_status_t hca_sink_attention_decode(const void *q, const float *sink, float softmax_scale, csa_cache_desc comp,
                                        const int32_t *n_comp, const void *swa_ring, int R, int W,
                                        const int32_t *q_pos, int B, int T, int m_hca, void *out, float *lse,
-                                       void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+                                       void *workspace, size_t workspace_bytes, int32_t *status,
+                                       cudaStream_t stream) {
     if (!q || !sink || !n_comp || !swa_ring || !q_pos || !out || !lse) return CSA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(swa_ring) || !aligned16(out) || !valid_cache(comp, B)) return CSA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(swa_ring) || !aligned16(out) || !valid_cache(comp, B) ||
+        !valid_status_word(status))
+        return CSA_ERR_INVALID_ARG;
     if (!valid_dims(B, T) || W < 1 || W > CSA_MAX_SWA_WINDOW || R < W || m_hca < 1 || !(softmax_scale > 0.f))
         return CSA_ERR_INVALID_ARG;
-    const size_t need = attention_workspace_bytes(B, T, comp.seq_capacity + CSA_MAX_SWA_WINDOW);
+    const size_t need = attention_workspace_bytes(B, T, comp.seq_capacity, W);
     if (need && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign)))
         return CSA_ERR_WORKSPACE;
     return cuda_status(launch_attention(q, sink, softmax_scale, comp, swa_ring, R, W, nullptr, nullptr, n_comp, m_hca,
-                                        q_pos, B, T, 0, true, comp.seq_capacity + CSA_MAX_SWA_WINDOW, out, lse,
-                                        workspace, workspace_bytes, device_error_word(), stream));
+                                        q_pos, B, T, comp.seq_capacity, true, out, lse, workspace, workspace_bytes,
+                                        status, stream));
 }
 
 csa_status_t csa_decode_step(const uint8_t *q_idx, const float *q_idx_scale, const float *w_idx,
@@ -254,12 +263,12 @@ csa_status_t csa_decode_step(const uint8_t *q_idx, const float *q_idx_scale, con
                              float softmax_scale, csa_cache_desc comp, const void *swa_ring, int R, int W,
                              const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap, int m, int k,
                              void *out, float *lse, int32_t *topk_idx, int32_t *topk_cnt, void *workspace,
-                             size_t workspace_bytes, cudaStream_t stream) {
+                             size_t workspace_bytes, int32_t *status, cudaStream_t stream) {
     // every argument of the three calls is checked before the first launch
     const csa_status_t a =
         csa::decode_step_arg_status(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q, sink, softmax_scale, comp,
                                     swa_ring, R, W, q_pos, n_comp, B, T, Ncap, m, k, out, lse, topk_idx,
-                                    workspace, workspace_bytes);
+                                    workspace, workspace_bytes, status);
     if (a != CSA_OK) return a;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     float *logits = reinterpret_cast<float *>(ws);
@@ -271,26 +280,34 @@ csa_status_t csa_decode_step(const uint8_t *q_idx, const float *q_idx_scale, con
     const size_t tk_bytes = align_up(topk_workspace_bytes(B, T, Ncap, k), kWsAlign);
     void *tk_ws = tk_bytes ? ws : nullptr;
     ws += tk_bytes;
-    const size_t at_bytes = align_up(attention_workspace_bytes(B, T, k + CSA_MAX_SWA_WINDOW), kWsAlign);
+    const size_t at_bytes = align_up(attention_workspace_bytes(B, T, k, CSA_MAX_SWA_WINDOW), kWsAlign);
     csa_status_t s = csa_indexer_logits(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q_pos, n_comp, B, T, Ncap, m,
-                                        logits, stream);
+                                        logits, status, stream);
     if (s != CSA_OK) return s;
-    s = csa_topk(logits, q_pos, n_comp, B, T, Ncap, m, k, idx, cnt, tk_ws, tk_bytes, stream);
+    s = csa_topk(logits, q_pos, n_comp, B, T, Ncap, m, k, idx, cnt, tk_ws, tk_bytes, status, stream);
     if (s != CSA_OK) return s;
     return csa_sink_attention_decode(q, sink, softmax_scale, comp, swa_ring, R, W, idx, cnt, q_pos, B, T, k, out, lse,
-                                     at_bytes ? ws : nullptr, at_bytes, stream);
+                                     at_bytes ? ws : nullptr, at_bytes, status, stream);
 }
 
-csa_status_t csa_read_device_error(int32_t *host_code, cudaStream_t stream) {
+csa_status_t csa_check_device_status(int32_t *status, int32_t *host_status, cudaStream_t stream) {
+    if (!status || !host_status || !aligned4(status) || !aligned4(host_status)) return CSA_ERR_INVALID_ARG;
+    if (cudaMemcpyAsync(host_status, status, sizeof(int32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return CSA_ERR_CUDA;
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), stream) != cudaSuccess) return CSA_ERR_CUDA;
+    return CSA_OK;
+}
+
+csa_status_t csa_read_device_error(int32_t *status, int32_t *host_code, cudaStream_t stream) {
     if (!host_code) return CSA_ERR_INVALID_ARG;
-    int *p = device_error_word();
-    if (!p) return CSA_ERR_CUDA;
-    int v = 0;
-    if (cudaMemcpyAsync(&v, p, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return CSA_ERR_CUDA;
-    if (cudaMemsetAsync(p, 0, sizeof(int), stream) != cudaSuccess) return CSA_ERR_CUDA;
+    int32_t v = 0;
+    const csa_status_t s = csa_check_device_status(status, &v, stream);
+    if (s != CSA_OK) return s;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return CSA_ERR_CUDA;
     *host_code = v;
     return CSA_OK;
 }
+
+void csa_debug_set_wait_limit_ns(uint64_t ns) { csa::set_wait_limit_ns(ns); }
 
 }  // extern "C"

@@ -63,7 +63,6 @@ constexpr int kQAtom = kHeads * 128;        // one 64-dim column block of Q: 128
 constexpr int kConvWarps = 8;               // load + dequantise warps
 constexpr int kLoPieces = 4;                // per thread: codes 0..255 of a record in 16-byte pieces, 4 threads a row
 constexpr int kHiPieces = 5;                // per thread: codes 256..447 and the rope dims (3 + 2 pieces)
-constexpr uint64_t kWaitNs = 1000000000ull; // 1 s per wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazy = 8.f;                // rescale only when the max grows by > 2^8
@@ -123,6 +122,7 @@ struct AttParams {
     __nv_bfloat16 *part_o;  // [rows, n_split, 128, 512] BF16 (n_split > 1)
     float2 *part_ml;        // [rows, n_split, 128] (max, sum) in log2 units
     int *err;
+    uint64_t wait_ns;  // limit of each bounded wait (drains keep kDrainWaitNs)
 };
 
 struct Unit {
@@ -250,7 +250,7 @@ attention_tc_kernel(const AttParams P) {
         *abort = 1;
     };
     auto wait = [&](uint64_t *bar, uint32_t parity) {
-        return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort, kWaitNs)) != 0;
+        return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort, P.wait_ns)) != 0;
     };
 
     if (role == kRoleProducer) {
@@ -394,7 +394,10 @@ attention_tc_kernel(const AttParams P) {
             ptx::mma_commit(&s.mma_done);
         }
         __syncwarp();
-        wait(&s.mma_done, 0);
+        // every MMA issued has finished with tensor and shared memory before
+        // the CTA frees them (not cut short by the abort flag)
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait_drain(&s.mma_done, 0, kDrainWaitNs)))
+            report_error(P.err, CSA_ERR_TIMEOUT);
     } else if (role == kRoleConvert) {
         // ------------------------------------------------------------ load + dequantise
         const int ct = convert_index(warp) * 32 + lane;  // 0..255
@@ -770,6 +773,7 @@ attention_combine_kernel(const __nv_bfloat16 *__restrict__ part_o, const float2 
 }
 
 // Splits per query so that about one CTA pair per two SMs is busy.
+// `max_candidates` bounds the candidates of any query (selected + window).
 int choose_splits(int rows, int max_candidates) {
     const int chunks = (max_candidates + kChunk - 1) / kChunk;
     const int target = cached_sm_count() / 2;
@@ -786,18 +790,21 @@ size_t split_bytes(int rows, int n_split) {
 
 }  // namespace
 
-size_t attention_workspace_bytes(int B, int T, int max_candidates) {
+// Workspace for queries of at most `max_selected` selected entries (top-k, or
+// the HCA capacity) and a window of at most W tokens. Monotone in both, so a
+// workspace sized with the largest window serves every smaller one.
+size_t attention_workspace_bytes(int B, int T, int max_selected, int W) {
     const int rows = B * T;
-    return split_bytes(rows, choose_splits(rows, max_candidates));
+    return split_bytes(rows, choose_splits(rows, max_selected + W));
 }
 
+// `k` = the top-k row length (CSA) or the per-sequence capacity (HCA).
 cudaError_t launch_attention(const void *q, const float *sink, float scale, const csa_cache_desc &comp,
                              const void *ring, int R, int W, const int32_t *topk_idx, const int32_t *topk_cnt,
                              const int32_t *n_comp, int m_hca, const int32_t *q_pos, int B, int T, int k, bool hca,
-                             int max_candidates, void *out, float *lse, void *ws, size_t ws_bytes, int *err,
-                             cudaStream_t stream) {
+                             void *out, float *lse, void *ws, size_t ws_bytes, int *err, cudaStream_t stream) {
     const int rows = B * T;
-    const int n_split = choose_splits(rows, max_candidates);
+    const int n_split = choose_splits(rows, k + W);
     AttParams P;
     P.q = static_cast<const __nv_bfloat16 *>(q);
     P.sink = sink;
@@ -813,13 +820,14 @@ cudaError_t launch_attention(const void *q, const float *sink, float scale, cons
     P.m_hca = m_hca;
     P.hca = hca ? 1 : 0;
     P.T = T;
-    P.k = k;
+    P.k = hca ? 0 : k;
     P.n_split = n_split;
     P.out = static_cast<__nv_bfloat16 *>(out);
     P.lse = lse;
     P.part_o = nullptr;
     P.part_ml = nullptr;
     P.err = err;
+    P.wait_ns = wait_limit_ns();
     if (n_split > 1) {
         const size_t need = split_bytes(rows, n_split);
         if (!ws || ws_bytes < need) return cudaErrorInvalidValue;
@@ -855,8 +863,6 @@ cudaError_t launch_attention(const void *q, const float *sink, float scale, cons
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
-
-int *error_word_for_current_device();
 
 // ------------------------------------------------------------------ allocation-free variant
 //
@@ -902,26 +908,18 @@ cudaError_t static_scratch_address(void **addr) {
 extern "C" CSA_API csa_status_t csa_sink_attention_decode_noalloc(
     const void *q, const float *sink, float softmax_scale, csa_cache_desc comp, const void *swa_ring, int R, int W,
     const int32_t *topk_idx, const int32_t *topk_cnt, const int32_t *q_pos, int B, int T, int k, void *out, float *lse,
-    cudaStream_t stream) {
+    int32_t *status, cudaStream_t stream) {
     using namespace csa;
-    const auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-    if (!q || !sink || !swa_ring || !topk_idx || !topk_cnt || !q_pos || !out || !lse) return CSA_ERR_INVALID_ARG;
-    if (!a16(q) || !a16(swa_ring) || !a16(out) || !comp.base || !a16(comp.base) || comp.n_records <= 0 ||
-        comp.seq_capacity <= 0)
-        return CSA_ERR_INVALID_ARG;
-    if (comp.block_table ? (!a16(comp.block_table) || comp.page_records <= 0 || comp.max_pages <= 0)
-                         : (comp.seq_stride < 0 || (B > 1 && comp.seq_stride < comp.seq_capacity)))
-        return CSA_ERR_INVALID_ARG;
-    if (B < 1 || T < 1 || T > CSA_MAX_TOKENS_PER_SEQ || (int64_t)B * T > 65535 || k < 1 || W < 1 ||
-        W > CSA_MAX_SWA_WINDOW || R < W || !(softmax_scale > 0.f))
-        return CSA_ERR_INVALID_ARG;
-    if (k > CSA_MAX_TOPK) return CSA_ERR_UNSUPPORTED;
-    const size_t need = attention_workspace_bytes(B, T, k + CSA_MAX_SWA_WINDOW);
+    // the same checks as csa_sink_attention_decode
+    const csa_status_t a = attention_arg_status(q, sink, softmax_scale, comp, swa_ring, R, W, topk_idx, topk_cnt,
+                                                q_pos, B, T, k, out, lse, status);
+    if (a != CSA_OK) return a;
+    const size_t need = attention_workspace_bytes(B, T, k, W);
     if (need > kStaticScratchBytes) return CSA_ERR_UNSUPPORTED;  // beyond the static scratch: use the workspace call
     void *scratch = nullptr;
     if (need && static_scratch_address(&scratch) != cudaSuccess) return CSA_ERR_CUDA;
     const cudaError_t e = launch_attention(q, sink, softmax_scale, comp, swa_ring, R, W, topk_idx, topk_cnt, nullptr,
-                                           1, q_pos, B, T, k, false, k + CSA_MAX_SWA_WINDOW, out, lse, scratch,
-                                           need ? kStaticScratchBytes : 0, error_word_for_current_device(), stream);
+                                           1, q_pos, B, T, k, false, out, lse, scratch,
+                                           need ? kStaticScratchBytes : 0, status, stream);
     return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
 }

@@ -24,6 +24,21 @@ constexpr int kIdxDim = CSA_INDEXER_DIM;
 
 // Host-side count of kernel launches issued by the library.
 void count_launch(int n = 1);
+// Time limit of the bounded waits in the tensor-core kernels (GPU global
+// time): one second unless a diagnostic call shortened it.
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;
+// Drain waits (copies and MMAs already issued) always keep the default.
+constexpr uint64_t kDrainWaitNs = kDefaultWaitNs;
+void set_wait_limit_ns(uint64_t ns);
+uint64_t wait_limit_ns();
+// Shared host-side argument checks.
+bool valid_cache(const csa_cache_desc &c, int B);
+bool valid_dims(int B, int T);
+bool valid_status_word(const int32_t *status);
+csa_status_t attention_arg_status(const void *q, const float *sink, float softmax_scale, const csa_cache_desc &comp,
+                                  const void *swa_ring, int R, int W, const int32_t *topk_idx,
+                                  const int32_t *topk_cnt, const int32_t *q_pos, int B, int T, int k,
+                                  const void *out, const float *lse, const int32_t *status);
 // Host-side per-device caches (thread-safe): SM count of the current device,
 // and the dynamic shared-memory opt-in of a kernel, set once per device.
 int cached_sm_count();
@@ -34,10 +49,10 @@ csa_status_t decode_step_arg_status(const uint8_t *q_idx, const float *q_idx_sca
                                     float softmax_scale, const csa_cache_desc &comp, const void *swa_ring, int R,
                                     int W, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap,
                                     int m, int k, const void *out, const float *lse, const int32_t *topk_idx,
-                                    const void *workspace, size_t workspace_bytes);
+                                    const void *workspace, size_t workspace_bytes, const int32_t *status);
 
-// Records first set a sticky code in the per-device error word; the first
-// error wins.
+// Records a code in the caller's status word (device memory); the first
+// error since the word was last cleared wins. No word: nothing is recorded.
 __device__ __forceinline__ void report_error(int *err, int code) {
     if (err) atomicCAS(err, 0, code);
 }

@@ -38,7 +38,6 @@ namespace csa {
 namespace {
 
 constexpr int kThreads = 320;  // producer, MMA, two 4-warp epilogue groups
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
 // Tile shape per tokens-per-sequence T: a tile is kHalves blocks of 128 keys
 // (one M = 128 MMA each). The MMA issuer's fixed per-tile cost (waits,
@@ -91,7 +90,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                   const float *__restrict__ q_scale, const float *__restrict__ w_idx,
                   const float *__restrict__ k_scale, const int32_t *__restrict__ q_pos,
-                  const int32_t *__restrict__ n_comp, int B, int Ncap, int m, float *__restrict__ logits, int *err) {
+                  const int32_t *__restrict__ n_comp, int B, int Ncap, int m, float *__restrict__ logits, int *err,
+                  uint64_t wait_ns) {
     using C = IdxCfg<T>;
     constexpr int N = C::N;
     constexpr int kHalves = C::kHalves, kTileKeys = C::kTileKeys, kStages = C::kStages, kTileBytes = C::kTileBytes;
@@ -168,7 +168,11 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     };
     // every lane of a warp waits; the outcome is made warp-uniform
     auto wait = [&](uint64_t *bar, uint32_t parity) {
-        return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort, kWaitLimitNs)) != 0;
+        return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort, wait_ns)) != 0;
+    };
+    // waits for work this CTA already issued: not cut short by the abort flag
+    auto drain = [&](uint64_t *bar, uint32_t parity) {
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait_drain(bar, parity, kDrainWaitNs))) report_error(err, CSA_ERR_TIMEOUT);
     };
 
     if (warp == 0) {
@@ -210,11 +214,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             __syncwarp();
             ++j;
         }
-        // drain: every issued copy has landed before the CTA may exit
+        // drain: every issued copy has landed before the CTA may exit (a copy
+        // older than the last kStages had its stage refilled, so it landed)
         for (uint32_t q = (j > kStages ? j - kStages : 0); q < j; ++q)
-            wait(&s.full[q % kStages], (q / kStages) & 1);
+            drain(&s.full[q % kStages], (q / kStages) & 1);
         for (uint32_t q = (u > 2 ? u - 2 : 0); q < u; ++q)
-            wait(&s.q_full[q & 1], (q >> 1) & 1);
+            drain(&s.q_full[q & 1], (q >> 1) & 1);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         int active_b = -1;
@@ -257,7 +262,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             ptx::mma_commit(&s.mma_done);
         }
         __syncwarp();
-        wait(&s.mma_done, 0);
+        drain(&s.mma_done, 0);  // every MMA issued has finished writing tensor memory
     } else {
         // ------------------------------------------------------------ epilogue
         // Two groups of 4 warps take alternate accumulated tiles (group g owns
@@ -464,7 +469,7 @@ cudaError_t launch_t(const uint8_t *q_idx, const float *q_scale, const float *w_
     cfg.numAttrs = 1;
     count_launch();
     e = cudaLaunchKernelEx(&cfg, indexer_tc_kernel<T>, kmap, qmap, q_scale, w_idx, k_scale, q_pos, n_comp, B, Ncap, m,
-                           logits, err);
+                           logits, err, wait_limit_ns());
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -124,7 +124,7 @@ csa_status_t csa_decode_step_host(csa_pipeline_t p, const uint8_t *h_q_idx, cons
                                   const uint8_t *k_idx, const float *k_idx_scale, const float *sink,
                                   float softmax_scale, csa_cache_desc comp, const void *swa_ring, int R, int W,
                                   const int32_t *n_comp, int Ncap, int m, int k, void *h_out, float *h_lse,
-                                  void *workspace, size_t workspace_bytes, int64_t *step_out) {
+                                  void *workspace, size_t workspace_bytes, int32_t *status, int64_t *step_out) {
     if (!p || !h_q_idx || !h_q_idx_scale || !h_w_idx || !h_q || !h_q_pos || !h_out || !h_lse)
         return CSA_ERR_INVALID_ARG;
     if (!on_pipeline_device(p)) return CSA_ERR_INVALID_ARG;
@@ -142,7 +142,7 @@ csa_status_t csa_decode_step_host(csa_pipeline_t p, const uint8_t *h_q_idx, cons
     const csa_status_t a =
         csa::decode_step_arg_status(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q, sink, softmax_scale, comp,
                                     swa_ring, R, W, q_pos, n_comp, B, T, Ncap, m, k, out, lse, nullptr, workspace,
-                                    workspace_bytes);
+                                    workspace_bytes, status);
     if (a != CSA_OK) return a;
 
     // host -> device, once step (i - depth) has finished reading this slot
@@ -165,7 +165,7 @@ csa_status_t csa_decode_step_host(csa_pipeline_t p, const uint8_t *h_q_idx, cons
     if (e != cudaSuccess) return CSA_ERR_CUDA;
     const csa_status_t st = csa_decode_step(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q, sink, softmax_scale,
                                             comp, swa_ring, R, W, q_pos, n_comp, B, T, Ncap, m, k, out, lse, nullptr,
-                                            nullptr, workspace, workspace_bytes, p->compute);
+                                            nullptr, workspace, workspace_bytes, status, p->compute);
     // computed[s] is recorded even after a failed launch, so that the slot's
     // later users do not wait on a stale record
     e = cudaEventRecord(p->computed[s], p->compute);

@@ -56,18 +56,51 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Limits below this are diagnostic: the wait then polls without the
+// hardware suspension of try_wait (which can outlast a short limit), so the
+// limit is what ends it.
+constexpr uint64_t kPollOnlyBelowNs = 1000000ull;
+
 // Bounded wait for the phase with the given parity. Gives up (returns false)
 // when `abort` is raised by another warp or after `limit_ns` of global time;
 // the caller then records the timeout and winds down.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, uint64_t limit_ns) {
+    const bool poll = limit_ns < kPollOnlyBelowNs;
+    if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0u) {  // first check right after the first retry, then every 64
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag, for draining work this thread's
+// CTA has already issued (TMA copies landing in shared memory, MMAs writing
+// tensor memory): such work completes by itself, so the CTA must wait for it
+// before it frees tensor memory or exits, whether or not another warp has
+// given up. Returns false only after `limit_ns` of global time.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 63u) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > limit_ns) return false;
-        }
+        if ((it & 63u) == 0u && globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 

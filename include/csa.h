@@ -17,16 +17,24 @@
  * Conventions for every call
  *  - Pointers are DEVICE pointers unless stated; the caller owns all memory.
  *    The library allocates no device memory (csa_pipeline_create makes a
- *    small host object, two streams and events). It keeps one device-side
- *    error word per device (see csa_read_device_error) and per-process kernel
- *    attributes.
+ *    small host object, two streams and events) and keeps no state beyond
+ *    per-process caches of kernel attributes, device properties and TMA
+ *    descriptors.
  *  - Calls are asynchronous on `stream`; none synchronises the device (the
  *    diagnostics and csa_pipeline_wait/sync/destroy block the host).
  *    Argument errors are detected on the host before any launch and returned
  *    as codes; launch failures return CSA_ERR_CUDA (cudaGetLastError).
- *  - Index or position data that would address memory outside a cache is
- *    detected in the kernels: the access is skipped and CSA_ERR_BAD_INDEX is
- *    recorded in the device error word. Kernels never trap.
+ *  - Status word: every compute call takes `status`, a caller-owned int32 in
+ *    device memory (4-byte aligned; NULL = do not record). Problems found
+ *    inside a kernel are recorded there, the first one winning (atomic
+ *    compare-and-swap from CSA_OK): an index or position that would address
+ *    memory outside a cache (the access is skipped: CSA_ERR_BAD_INDEX) and a
+ *    bounded wait that expired (the kernel winds down: CSA_ERR_TIMEOUT).
+ *    Kernels never trap. The word is read without stalling the stream by
+ *    csa_check_device_status ("ROADMAP -- Stage E", section E4: no
+ *    synchronisation on the decode path; return codes instead). Calls that
+ *    share a word share its first-error-wins slot; give concurrent streams
+ *    their own words.
  *  - Shapes fixed by the method: H = 128 query heads, latent D = 512 = 448
  *    FP8 E4M3 "nope" dims + 64 BF16 rope dims, indexer Hi = 64 heads x Di = 128
  *    FP8 dims. Tensors are dense row-major in the order of their index lists.
@@ -127,7 +135,8 @@ CSA_API size_t csa_workspace_bytes(csa_op_t op, int B, int T, int Ncap, int k);
 CSA_API csa_status_t csa_indexer_logits(const uint8_t *q_idx, const float *q_idx_scale, const float *w_idx,
                                 const uint8_t *k_idx, const float *k_idx_scale,
                                 const int32_t *q_pos, const int32_t *n_comp,
-                                int B, int T, int Ncap, int m, float *logits, cudaStream_t stream);
+                                int B, int T, int Ncap, int m, float *logits, int32_t *status,
+                                cudaStream_t stream);
 
 /* Step 2 -- top-k of the indexer logits over the visible entries ("DSV4
  * Audit", section B2 and "ROADMAP -- Stage E", section E7: top-k per query
@@ -140,7 +149,7 @@ CSA_API csa_status_t csa_indexer_logits(const uint8_t *q_idx, const float *q_idx
  * The workspace may be NULL when csa_workspace_bytes(CSA_OP_TOPK, ...) is 0. */
 CSA_API csa_status_t csa_topk(const float *logits, const int32_t *q_pos, const int32_t *n_comp,
                       int B, int T, int Ncap, int m, int k, int32_t *topk_idx, int32_t *topk_cnt,
-                      void *workspace, size_t workspace_bytes, cudaStream_t stream);
+                      void *workspace, size_t workspace_bytes, int32_t *status, cudaStream_t stream);
 
 /* Step 3, standalone -- packed candidate records ("DSV4 Audit", section A3:
  * the query attends to [top-k compressed entries] ++ [SWA window]; a token in
@@ -156,7 +165,8 @@ CSA_API csa_status_t csa_topk(const float *logits, const int32_t *q_pos, const i
  * window of every query token (R >= W + T - 1 for consecutive tokens). */
 CSA_API csa_status_t csa_gather_swa(csa_cache_desc comp, const void *swa_ring, int R, int W,
                             const int32_t *topk_idx, const int32_t *topk_cnt, const int32_t *q_pos,
-                            int B, int T, int k, void *kv_out, int32_t *kv_cnt, cudaStream_t stream);
+                            int B, int T, int k, void *kv_out, int32_t *kv_cnt, int32_t *status,
+                            cudaStream_t stream);
 
 /* Step 4 -- sink-merged attention over [top-k entries] ++ [SWA window]
  * ("DSV4 Inference Kernel" README, Architecture: one 512-d latent per entry
@@ -177,7 +187,7 @@ CSA_API csa_status_t csa_sink_attention_decode(const void *q, const float *sink,
                                        const int32_t *topk_idx, const int32_t *topk_cnt,
                                        const int32_t *q_pos, int B, int T, int k,
                                        void *out, float *lse, void *workspace, size_t workspace_bytes,
-                                       cudaStream_t stream);
+                                       int32_t *status, cudaStream_t stream);
 
 /* HCA variant ("DSV4 Inference Kernel" README, Architecture, m' = 128;
  * "ROADMAP -- Stage E", section E1, gather of all compressed entries):
@@ -187,7 +197,8 @@ CSA_API csa_status_t hca_sink_attention_decode(const void *q, const float *sink,
                                        csa_cache_desc comp, const int32_t *n_comp,
                                        const void *swa_ring, int R, int W, const int32_t *q_pos,
                                        int B, int T, int m_hca, void *out, float *lse,
-                                       void *workspace, size_t workspace_bytes, cudaStream_t stream);
+                                       void *workspace, size_t workspace_bytes, int32_t *status,
+                                       cudaStream_t stream);
 
 /* Allocation-free variant of csa_sink_attention_decode (the pages have no
  * counterpart; it exists for callers of this library that cannot allocate
@@ -203,8 +214,10 @@ CSA_API csa_status_t hca_sink_attention_decode(const void *q, const float *sink,
  *    array's device address once (cudaGetSymbolAddress) and caches it; make
  *    that first call before any stream capture.
  *  - Sizes whose partials exceed the array return CSA_ERR_UNSUPPORTED (use
- *    csa_sink_attention_decode with a workspace instead); the limit is
- *    csa_workspace_bytes(CSA_OP_ATTENTION, B, T, Ncap, k) <= 16 MiB.
+ *    csa_sink_attention_decode with a workspace instead); every size with
+ *    csa_workspace_bytes(CSA_OP_ATTENTION, B, T, Ncap, k) <= 16 MiB fits.
+ *  - Argument checks and their status codes are those of
+ *    csa_sink_attention_decode; `status` is the caller's status word.
  *  - Every call shares the array and leaves its contents behind; nothing in it
  *    needs to start at zero. Calls that overlap on the GPU (concurrent streams)
  *    race on the array: serialise them. */
@@ -212,7 +225,7 @@ CSA_API csa_status_t csa_sink_attention_decode_noalloc(const void *q, const floa
                                                        csa_cache_desc comp, const void *swa_ring, int R, int W,
                                                        const int32_t *topk_idx, const int32_t *topk_cnt,
                                                        const int32_t *q_pos, int B, int T, int k, void *out,
-                                                       float *lse, cudaStream_t stream);
+                                                       float *lse, int32_t *status, cudaStream_t stream);
 
 /* One CSA decode step: csa_indexer_logits -> csa_topk ->
  * csa_sink_attention_decode on one stream. Logits, indices and attention
@@ -227,7 +240,7 @@ CSA_API csa_status_t csa_decode_step(const uint8_t *q_idx, const float *q_idx_sc
                              const int32_t *q_pos, const int32_t *n_comp,
                              int B, int T, int Ncap, int m, int k,
                              void *out, float *lse, int32_t *topk_idx, int32_t *topk_cnt,
-                             void *workspace, size_t workspace_bytes, cudaStream_t stream);
+                             void *workspace, size_t workspace_bytes, int32_t *status, cudaStream_t stream);
 
 /* Host-I/O decode pipeline (the pages have no counterpart; it serves callers
  * whose query-side inputs arrive in, and whose results go back to, host
@@ -280,7 +293,7 @@ CSA_API csa_status_t csa_decode_step_host(csa_pipeline_t pipeline, const uint8_t
                                           const float *sink, float softmax_scale, csa_cache_desc comp,
                                           const void *swa_ring, int R, int W, const int32_t *n_comp, int Ncap,
                                           int m, int k, void *h_out, float *h_lse, void *workspace,
-                                          size_t workspace_bytes, int64_t *step_out);
+                                          size_t workspace_bytes, int32_t *status, int64_t *step_out);
 
 /* Blocks the host until step `step` (an ordinal returned by
  * csa_decode_step_host) has its results in host memory and its host inputs
@@ -295,10 +308,34 @@ CSA_API csa_status_t csa_pipeline_sync(csa_pipeline_t pipeline);
  * object (not the staging memory, which the caller owns). NULL is a no-op. */
 CSA_API csa_status_t csa_pipeline_destroy(csa_pipeline_t pipeline);
 
-/* Reads and clears the current device's error word (CSA_OK or the first
- * CSA_ERR_TIMEOUT / CSA_ERR_BAD_INDEX recorded by a kernel). Blocking: it
- * synchronises `stream`. For tests and diagnostics, not for the hot path. */
-CSA_API csa_status_t csa_read_device_error(int32_t *host_code, cudaStream_t stream);
+/* Reads and clears a status word without synchronising ("ROADMAP -- Stage
+ * E", section E4: no synchronisation on the decode path; errors come back as
+ * codes). Enqueues on `stream` a copy of *status (device) into *host_status
+ * (host memory; page-locked memory keeps the copy asynchronous, pageable
+ * memory makes the runtime stage it) followed by a reset of *status to
+ * CSA_OK. The value in *host_status is valid once the stream has passed this
+ * point (an event recorded after the call, or a synchronisation chosen by
+ * the caller): CSA_OK, or the first CSA_ERR_TIMEOUT / CSA_ERR_BAD_INDEX that
+ * a kernel recorded in the word since the previous reset. Work enqueued on
+ * the stream after this call records into a clean word. Legal inside CUDA
+ * graph capture. CSA_ERR_INVALID_ARG for a null or misaligned pointer,
+ * CSA_ERR_CUDA if the copy or the reset cannot be enqueued. */
+CSA_API csa_status_t csa_check_device_status(int32_t *status, int32_t *host_status, cudaStream_t stream);
+
+/* Blocking convenience for tests and diagnostics: csa_check_device_status
+ * into a local, then cudaStreamSynchronize(stream), then *host_code = the
+ * value read. Not for the decode path. */
+CSA_API csa_status_t csa_read_device_error(int32_t *status, int32_t *host_code, cudaStream_t stream);
+
+/* Diagnostic: sets the time limit of the bounded waits inside the tensor-core
+ * kernels (indexer and attention) for launches made after this call, in
+ * nanoseconds of GPU global time; 0 restores the default of one second. A
+ * wait that reaches the limit records CSA_ERR_TIMEOUT in the status word and
+ * the kernel winds down: it drains its own copies and MMAs already in flight
+ * (those waits keep the one-second limit), frees its tensor memory and exits.
+ * Exists so that tests can drive the timeout path without hanging or faulting
+ * anything; process-wide, not for the decode path. */
+CSA_API void csa_debug_set_wait_limit_ns(uint64_t ns);
 
 /* Static description of a status code. */
 CSA_API const char *csa_status_string(csa_status_t status);

@@ -57,30 +57,30 @@ def test_host_validation_rejects_before_launch(lib):
     P = C.c_void_p
     fake = P(0x1000)  # never dereferenced: validation fails first
     # null pointers
-    assert lib.csa_indexer_logits(None, None, None, None, None, None, None, 1, 1, 8, 4, None, None) == csd.ERR_INVALID_ARG
+    assert lib.csa_indexer_logits(None, None, None, None, None, None, None, 1, 1, 8, 4, None, None, None) == csd.ERR_INVALID_ARG
     # T beyond the supported maximum
-    assert lib.csa_indexer_logits(fake, fake, fake, fake, fake, fake, fake, 1, 5, 8, 4, fake, None) == csd.ERR_INVALID_ARG
+    assert lib.csa_indexer_logits(fake, fake, fake, fake, fake, fake, fake, 1, 5, 8, 4, fake, None, None) == csd.ERR_INVALID_ARG
     # misaligned logits pointer
-    assert lib.csa_indexer_logits(fake, fake, fake, fake, fake, fake, fake, 1, 1, 8, 4, P(0x1004), None) == csd.ERR_INVALID_ARG
+    assert lib.csa_indexer_logits(fake, fake, fake, fake, fake, fake, fake, 1, 1, 8, 4, P(0x1004), None, None) == csd.ERR_INVALID_ARG
     # k larger than the capacity / the maximum
-    assert lib.csa_topk(fake, fake, fake, 1, 1, 8, 4, 9, fake, fake, None, 0, None) == csd.ERR_UNSUPPORTED
-    assert lib.csa_topk(fake, fake, fake, 1, 1, 10000, 4, 4096, fake, fake, None, 0, None) == csd.ERR_UNSUPPORTED
+    assert lib.csa_topk(fake, fake, fake, 1, 1, 8, 4, 9, fake, fake, None, 0, None, None) == csd.ERR_UNSUPPORTED
+    assert lib.csa_topk(fake, fake, fake, 1, 1, 10000, 4, 4096, fake, fake, None, 0, None, None) == csd.ERR_UNSUPPORTED
     # cache descriptor without records, window larger than the ring
     bad = csd.csa_cache_desc()
-    assert lib.csa_gather_swa(bad, fake, 128, 128, fake, fake, fake, 1, 1, 4, fake, fake, None) == csd.ERR_INVALID_ARG
+    assert lib.csa_gather_swa(bad, fake, 128, 128, fake, fake, fake, 1, 1, 4, fake, fake, None, None) == csd.ERR_INVALID_ARG
     good = csd.csa_cache_desc()
     good.base, good.n_records, good.seq_stride, good.seq_capacity = 0x1000, 10, 10, 10
-    assert lib.csa_gather_swa(good, fake, 64, 128, fake, fake, fake, 1, 1, 4, fake, fake, None) == csd.ERR_INVALID_ARG
+    assert lib.csa_gather_swa(good, fake, 64, 128, fake, fake, fake, 1, 1, 4, fake, fake, None, None) == csd.ERR_INVALID_ARG
     # contiguous mode with overlapping sequences
     over = csd.csa_cache_desc()
     over.base, over.n_records, over.seq_stride, over.seq_capacity = 0x1000, 100, 5, 10
-    assert lib.csa_gather_swa(over, fake, 128, 128, fake, fake, fake, 2, 1, 4, fake, fake, None) == csd.ERR_INVALID_ARG
+    assert lib.csa_gather_swa(over, fake, 128, 128, fake, fake, fake, 2, 1, 4, fake, fake, None, None) == csd.ERR_INVALID_ARG
     # non-positive softmax scale
     assert lib.csa_sink_attention_decode(fake, fake, C.c_float(0.0), good, fake, 128, 128, fake, fake, fake, 1, 1, 4,
-                                         fake, fake, None, 0, None) == csd.ERR_INVALID_ARG
+                                         fake, fake, None, 0, None, None) == csd.ERR_INVALID_ARG
     # decode step without workspace
     assert lib.csa_decode_step(fake, fake, fake, fake, fake, fake, fake, C.c_float(0.1), good, fake, 128, 128, fake,
-                               fake, 1, 1, 10, 4, 4, fake, fake, None, None, None, 0, None) == csd.ERR_WORKSPACE
+                               fake, 1, 1, 10, 4, 4, fake, fake, None, None, None, 0, None, None) == csd.ERR_WORKSPACE
 
 
 def test_pipeline_staging_sizes(lib):
@@ -113,7 +113,7 @@ def test_pipeline_validation_before_any_cuda_call(lib):
     fake = P(0x1000)
     step = C.c_int64(-1)
     assert lib.csa_decode_step_host(None, *([fake] * 8), C.c_float(0.1), good, fake, 128, 128, fake, 10, 4, 4,
-                                    fake, fake, fake, 1 << 20, C.byref(step)) == csd.ERR_INVALID_ARG
+                                    fake, fake, fake, 1 << 20, None, C.byref(step)) == csd.ERR_INVALID_ARG
     assert step.value == -1
     assert lib.csa_pipeline_wait(None, 0) == csd.ERR_INVALID_ARG
     assert lib.csa_pipeline_sync(None) == csd.ERR_INVALID_ARG
@@ -126,7 +126,7 @@ def test_decode_step_checks_every_argument_before_launching(lib):
     good.base, good.n_records, good.seq_stride, good.seq_capacity = 0x1000, 10, 10, 10
     ws = csd.csa_workspace_bytes(csd.OP_DECODE_STEP, 1, 1, 10, 4)
     args = [fake] * 7 + [C.c_float(0.1), good, fake, 128, 128, fake, fake, 1, 1, 10, 4, 4, fake, fake, None, None,
-                         fake, ws, None]
+                         fake, ws, None, None]
     # a null sink (an attention argument) is reported before the indexer launches
     bad = list(args)
     bad[6] = None
@@ -139,6 +139,51 @@ def test_decode_step_checks_every_argument_before_launching(lib):
     bad = list(args)
     bad[19] = C.c_void_p(0x1004)
     assert lib.csa_decode_step(*bad) == csd.ERR_INVALID_ARG
+
+
+def test_status_word_checks(lib):
+    P = C.c_void_p
+    host = C.c_int32(7)
+    # null or misaligned words are rejected before anything is enqueued
+    assert lib.csa_check_device_status(None, C.byref(host), None) == csd.ERR_INVALID_ARG
+    assert lib.csa_check_device_status(P(0x1002), C.byref(host), None) == csd.ERR_INVALID_ARG
+    assert lib.csa_check_device_status(P(0x1000), None, None) == csd.ERR_INVALID_ARG
+    assert lib.csa_read_device_error(None, C.byref(host), None) == csd.ERR_INVALID_ARG
+    assert host.value == 7
+    # a misaligned status word is an argument error of every compute call
+    fake = P(0x1000)
+    assert lib.csa_indexer_logits(fake, fake, fake, fake, fake, fake, fake, 1, 1, 8, 4, fake, P(0x1001),
+                                  None) == csd.ERR_INVALID_ARG
+    assert lib.csa_topk(fake, fake, fake, 1, 1, 8, 4, 4, fake, fake, None, 0, P(0x1002), None) == csd.ERR_INVALID_ARG
+    good = csd.csa_cache_desc()
+    good.base, good.n_records, good.seq_stride, good.seq_capacity = 0x1000, 10, 10, 10
+    assert lib.csa_sink_attention_decode(fake, fake, C.c_float(0.1), good, fake, 128, 128, fake, fake, fake, 1, 1, 4,
+                                         fake, fake, None, 0, P(0x1003), None) == csd.ERR_INVALID_ARG
+    assert lib.csa_sink_attention_decode_noalloc(fake, fake, C.c_float(0.1), good, fake, 128, 128, fake, fake, fake,
+                                                 1, 1, 4, fake, fake, P(0x1003), None) == csd.ERR_INVALID_ARG
+
+
+def test_noalloc_rejects_like_the_workspace_call(lib):
+    """The allocation-free attention entry runs the same host checks as the
+    workspace entry: each bad argument gets the same status from both."""
+    fake = C.c_void_p(0x1000)
+    good = csd.csa_cache_desc()
+    good.base, good.n_records, good.seq_stride, good.seq_capacity = 0x1000, 10, 10, 10
+    bad_cache = csd.csa_cache_desc()
+    over = csd.csa_cache_desc()
+    over.base, over.n_records, over.seq_stride, over.seq_capacity = 0x1000, 100, 5, 10
+    cases = [
+        dict(q=None), dict(comp=bad_cache), dict(comp=over, B=2), dict(W=600, R=600), dict(R=64),
+        dict(scale=0.0), dict(k=4096), dict(T=5), dict(out=C.c_void_p(0x1008)),
+    ]
+    for c in cases:
+        a = dict(q=fake, comp=good, R=128, W=128, B=1, T=1, k=4, out=fake, scale=0.1)
+        a.update(c)
+        common = (a["q"], fake, C.c_float(a["scale"]), a["comp"], fake, a["R"], a["W"], fake, fake, fake, a["B"],
+                  a["T"], a["k"], a["out"], fake)
+        ws_status = lib.csa_sink_attention_decode(*common, None, 0, None, None)
+        na_status = lib.csa_sink_attention_decode_noalloc(*common, None, None)
+        assert ws_status == na_status != csd.OK, c
 
 
 def test_product_path_does_not_import_the_oracle():

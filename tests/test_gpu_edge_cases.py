@@ -1,8 +1,9 @@
 """GPU edge cases against the oracle: ragged capacities spanning several tiles
 with a ragged tail, T up to 4 with per-token visible ranges, empty visible
 ranges, windows shorter than W, k above the visible count, paged caches with
-a shuffled block table, heavy ties in top-k, a -inf sink, and indices outside
-the cache (reported through the device error word, never dereferenced)."""
+a shuffled block table, heavy ties in top-k, a -inf sink, indices outside
+the cache (reported through the caller's status word, never dereferenced),
+and bounded waits made to expire (reported, and the device stays usable)."""
 import math
 import os
 
@@ -154,15 +155,56 @@ def test_single_candidate_with_minus_inf_sink(cuda_lib):
 
 
 def test_out_of_cache_index_is_reported_not_read(cuda_lib):
+    """Indices outside the cache are skipped and reported in the caller's
+    status word, read back with the asynchronous check after a caller-side
+    synchronisation (an event), also from inside a captured CUDA graph."""
     x = _custom(1, 1, 64, 4, [[1000]], [64])
     idx = torch.tensor([[[3, 64, 1 << 30, -5]]], dtype=torch.int32, device="cuda")
     cnt = torch.tensor([[4]], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    host = torch.full((1,), -1, dtype=torch.int32).pin_memory()
+    comp = _cache(cuda_lib, x)
+
+    def synced(fn):
+        fn()
+        ev = torch.cuda.Event()
+        ev.record()
+        ev.synchronize()
+        return int(host.item())
+
+    assert synced(lambda: cuda_lib.csa_check_device_status(host, status=status)) == 0
+    cuda_lib.csa_sink_attention_decode(x.q, x.sink, SCALE, comp, x.ring, 128, idx, cnt, x.q_pos, status=status)
+    assert synced(lambda: cuda_lib.csa_check_device_status(host, status=status)) == cuda_lib.ERR_BAD_INDEX
+    assert synced(lambda: cuda_lib.csa_check_device_status(host, status=status)) == 0   # the check cleared it
+    cuda_lib.csa_gather_swa(comp, x.ring, 128, idx, cnt, x.q_pos, status=status)
+    assert synced(lambda: cuda_lib.csa_check_device_status(host, status=status)) == cuda_lib.ERR_BAD_INDEX
+    # the binding's default word was not touched by calls given their own
     assert cuda_lib.csa_read_device_error() == 0
-    cuda_lib.csa_sink_attention_decode(x.q, x.sink, SCALE, _cache(cuda_lib, x), x.ring, 128, idx, cnt, x.q_pos)
-    assert cuda_lib.csa_read_device_error() == cuda_lib.ERR_BAD_INDEX
-    cuda_lib.csa_gather_swa(_cache(cuda_lib, x), x.ring, 128, idx, cnt, x.q_pos)
-    assert cuda_lib.csa_read_device_error() == cuda_lib.ERR_BAD_INDEX
-    assert cuda_lib.csa_read_device_error() == 0   # reading clears the word
+    # captured: attention, then the status check, replayed as one graph
+    out = torch.empty_like(x.q)
+    lse = torch.empty((1, 1, 128), dtype=torch.float32, device="cuda")
+    ws = cuda_lib.workspace(cuda_lib.OP_ATTENTION, 1, 1, 64, 4, "cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):   # warm-up outside capture (host-side caches)
+        cuda_lib.csa_sink_attention_decode(x.q, x.sink, SCALE, comp, x.ring, 128, idx, cnt, x.q_pos, out=out, lse=lse,
+                                           ws=ws, status=status)
+        cuda_lib.csa_check_device_status(host, status=status)
+    s.synchronize()
+    host.fill_(-1)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        cuda_lib.csa_sink_attention_decode(x.q, x.sink, SCALE, comp, x.ring, 128, idx, cnt, x.q_pos, out=out, lse=lse,
+                                           ws=ws, status=status, stream=s)
+        cuda_lib.csa_check_device_status(host, status=status, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(host.item()) == cuda_lib.ERR_BAD_INDEX
+    good = torch.tensor([[[3, 7, 9, 11]]], dtype=torch.int32, device="cuda")
+    idx.copy_(good)
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(host.item()) == 0
 
 
 def test_late_dominant_candidate_forces_rescale(cuda_lib):
@@ -190,3 +232,47 @@ def test_late_dominant_candidate_forces_rescale(cuda_lib):
     tol = lse_bounds_for_rows(x, rows, lambda r: gi[r][:gc[r]], SCALE)
     check_attention(out.float().cpu().numpy().reshape(-1, 128, 512)[rows], lse.cpu().numpy().reshape(-1, 128)[rows],
                     oo.reshape(-1, 128, 512)[rows], ol.reshape(-1, 128)[rows], "rescale", tol)
+
+
+def test_expired_waits_are_reported_and_the_next_calls_are_correct(cuda_lib):
+    """The tensor-core kernels' bounded waits, shortened to 1 ns, expire: the
+    kernels record CSA_ERR_TIMEOUT, drain what they issued, free tensor memory
+    and exit; with the default limit restored, the same calls on the same
+    device give the results they gave before, which match the oracle."""
+    x = synth.generate("csa_b8_ctx16k32k_k512", seed=0, device="cuda")
+    wl = x.wl
+    comp = _cache(cuda_lib, x)
+    lg0, idx0, cnt0 = _pipeline(cuda_lib, x)
+    out0, lse0 = cuda_lib.csa_sink_attention_decode(x.q, x.sink, SCALE, comp, x.ring, wl.W, idx0, cnt0, x.q_pos)
+    torch.cuda.synchronize()
+    assert cuda_lib.csa_read_device_error() == 0
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cuda_lib.csa_debug_set_wait_limit_ns(1)
+    try:
+        lg1 = cuda_lib.csa_indexer_logits(x.q_idx, x.q_idx_scale, x.w_idx, x.k_idx, x.k_idx_scale, x.q_pos, x.n_comp,
+                                          wl.m, status=status)
+        torch.cuda.synchronize()
+        idx_status = cuda_lib.csa_read_device_error(status=status)
+        cuda_lib.csa_sink_attention_decode(x.q, x.sink, SCALE, comp, x.ring, wl.W, idx0, cnt0, x.q_pos, status=status)
+        torch.cuda.synchronize()
+        att_status = cuda_lib.csa_read_device_error(status=status)
+    finally:
+        cuda_lib.csa_debug_set_wait_limit_ns(0)
+    assert (idx_status, att_status) == (cuda_lib.ERR_TIMEOUT, cuda_lib.ERR_TIMEOUT)
+    del lg1
+    # the device is usable and the calls are again exact
+    lg2, idx2, cnt2 = _pipeline(cuda_lib, x)
+    out2, lse2 = cuda_lib.csa_sink_attention_decode(x.q, x.sink, SCALE, comp, x.ring, wl.W, idx2, cnt2, x.q_pos,
+                                                    status=status)
+    torch.cuda.synchronize()
+    assert cuda_lib.csa_read_device_error(status=status) == 0
+    assert torch.equal(lg2, lg0) and torch.equal(idx2, idx0) and torch.equal(cnt2, cnt0)
+    assert torch.equal(out2, out0) and torch.equal(lse2, lse0)
+    rows = [0, 5]
+    oo, ol = oracle.csa_attention(x.q.view(torch.int16).cpu(), x.sink.cpu(), SCALE, oracle_cache(x),
+                                  x.ring.cpu().numpy(), wl.W, idx2.cpu(), cnt2.cpu(), x.q_pos.cpu(), threads=THREADS,
+                                  rows=rows)
+    gi, gc = idx2.cpu().numpy().reshape(-1, wl.k), cnt2.cpu().numpy().reshape(-1)
+    tol = lse_bounds_for_rows(x, rows, lambda r: gi[r][:gc[r]], SCALE)
+    check_attention(out2.float().cpu().numpy().reshape(-1, 128, 512)[rows], lse2.cpu().numpy().reshape(-1, 128)[rows],
+                    oo.reshape(-1, 128, 512)[rows], ol.reshape(-1, 128)[rows], "after timeout", tol)
