@@ -34,7 +34,7 @@ METRIC = "CSA decode tokens/s at 128K ctx; achieved HBM GB/s and % of roofline"
 UNIT = "tokens/s"
 SCALE = 1.0 / math.sqrt(512)
 N_COPIES = 3  # rotating input copies: each step's inputs are not L2-resident
-IDX_SAMPLE_EVERY = 4  # timed-region steps whose indexer launch is bracketed by events
+SAMPLE_EVERY = 8  # timed-region steps: the indexer is bracketed by events on steps i % 8 == 0, the attention on i % 8 == 4
 
 
 def parse():
@@ -47,7 +47,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--report-configs", action="store_true",
-                    help="print a per-kernel table for every workload instead of the benchmark line")
+                    help="print one JSON line of per-kernel times for every workload instead of the benchmark line")
+    ap.add_argument("--graph-replay", type=int, default=0, metavar="LAYERS",
+                    help="time LAYERS decode steps (one per layer, each with its own paged cache) as direct calls "
+                         "and as one replayed CUDA graph, on --workload (default: the 1K-context one)")
     return ap.parse_args()
 
 
@@ -154,15 +157,16 @@ def indexer_bytes(x) -> int:
     return keys + wl.B * wl.T * (per_tok + 4 * wl.ncap)
 
 
-def attention_bytes(cnt, x) -> int:
-    """Bytes the attention must move: 592 B per candidate record per query
-    (top-k entries + SWA window), the BF16 query and output rows (128 KB
-    each) and the fp32 LSE."""
+def attention_work(cnt, x) -> tuple[int, float]:
+    """Bytes the attention must move and the flops it must do: 592 B and
+    2 x 128 x 512 x 2 flops (QK and PV) per candidate record per query (top-k
+    entries + SWA window), plus the BF16 query and output rows (128 KB each)
+    and the fp32 LSE."""
     import numpy as np
     q_pos = x.q_pos.cpu().numpy().reshape(-1)
     nswa = np.minimum(q_pos + 1, x.wl.W)
     cands = int(cnt.sum()) + int(nswa.sum())
-    return cands * 592 + x.wl.B * x.wl.T * (2 * 128 * 512 * 2 + 128 * 4)
+    return cands * 592 + x.wl.B * x.wl.T * (2 * 128 * 512 * 2 + 128 * 4), 262144.0 * cands
 
 
 def load_peaks() -> dict:
@@ -281,13 +285,15 @@ def run_ours(args, rank, world, local_rank):
     clocks = ClockSampler(uuid)
     clocks.start()
     time.sleep(0.3)
-    # Events inside the timed loop bracket only the indexer (the roofline
-    # kernel), and only on every IDX_SAMPLE_EVERY-th step: an event between two
-    # kernels stops the next one from being set up while its predecessor
-    # drains (programmatic dependent launch), which costs ~9 us per bracketed
-    # step on the 128K workload.
-    sampled = [i for i in range(args.steps) if i % IDX_SAMPLE_EVERY == 0]
-    ev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for i in sampled}
+    # Events inside the timed loop bracket the two roofline kernels, each on
+    # one step in SAMPLE_EVERY (the indexer on steps i % 8 == 0, the attention
+    # with its split combine on steps i % 8 == 4): an event between two kernels
+    # stops the next one from being set up while its predecessor drains
+    # (programmatic dependent launch), which costs a few us per bracket.
+    ev_idx = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for i in range(args.steps) if i % SAMPLE_EVERY == 0}
+    ev_att = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for i in range(args.steps) if i % SAMPLE_EVERY == SAMPLE_EVERY // 2}
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # keep the GPU busy right up to the timed region (clock samples stay meaningful)
     with torch.cuda.stream(stream):
@@ -302,14 +308,19 @@ def run_ours(args, rank, world, local_rank):
         start.record(stream)
         for i in range(args.steps):
             r = runners[i % N_COPIES]
-            if i in ev:
-                ev[i][0].record(stream)
+            if i in ev_idx:
+                ev_idx[i][0].record(stream)
                 r.indexer()
-                ev[i][1].record(stream)
+                ev_idx[i][1].record(stream)
             else:
                 r.indexer()
             r.topk()
-            r.attention()
+            if i in ev_att:
+                ev_att[i][0].record(stream)
+                r.attention()
+                ev_att[i][1].record(stream)
+            else:
+                r.attention()
         end.record(stream)
     torch.cuda.synchronize(dev)
     t1 = time.time()
@@ -318,7 +329,8 @@ def run_ours(args, rank, world, local_rank):
     time.sleep(0.1)
     clocks.stop()
     total_ms = start.elapsed_time(end)
-    t_idx = [a.elapsed_time(b) for a, b in ev.values()]
+    t_idx = [a.elapsed_time(b) for a, b in ev_idx.values()]
+    t_att_live = [a.elapsed_time(b) for a, b in ev_att.values()]
     # per-kernel breakdown (after the timed region, same inputs): events around
     # every kernel, which serialises their boundaries
     bev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(min(args.steps, 12))]
@@ -336,15 +348,12 @@ def run_ours(args, rank, world, local_rank):
     value = job_throughput(wl.B * wl.T * args.steps, world, total_ms)
     peaks = load_peaks()
     idx_bytes = indexer_bytes(base)
-    att_bytes = attention_bytes(runners[0].cnt.cpu().numpy(), base)
+    att_bytes, att_flops = attention_work(runners[0].cnt.cpu().numpy(), base)
     idx_ms = statistics.mean(t_idx)
-    achieved = idx_bytes / (idx_ms / 1e3) / 1e9
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "indexer_traffic.json")
-    if os.path.exists(prof):
-        d = json.load(open(prof))
-        if d.get("workload") == name and d.get("kernel_source_hash") == kernel_hash():
-            traffic = d.get("dram_bytes_per_launch")
+    att_ms = statistics.mean(t_att_live) if t_att_live else statistics.mean(t_att)
+    idx_gbs = idx_bytes / (idx_ms / 1e3) / 1e9
+    att_gbs = att_bytes / (att_ms / 1e3) / 1e9
+    att_tflops = att_flops / (att_ms / 1e3) / 1e12
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -356,15 +365,25 @@ def run_ours(args, rank, world, local_rank):
                    "l2": f"inputs larger than L2: {N_COPIES} rotating copies, each step reads a different one",
                    "parallelism": f"replicas x{world}"},
         "kernel_ms": {"indexer": round(idx_ms, 5), "topk": round(statistics.mean(t_topk), 5),
-                      "attention": round(statistics.mean(t_att), 5),
-                      "source": f"indexer: events around every {IDX_SAMPLE_EVERY}th launch in the timed region "
-                                f"({len(t_idx)} launches); topk, attention (+ split combine): a breakdown pass "
-                                "after it with events around every kernel"},
-        "roofline": {"kernel": "csa_indexer_logits", "bound": "hbm", "achieved": round(achieved, 1),
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "peak_source": peaks["source"], "traffic": traffic, "algorithmic_bytes": idx_bytes},
-        "attention_roofline": {"achieved": round(att_bytes / (statistics.mean(t_att) / 1e3) / 1e9, 1),
-                               "unit": "GB/s", "algorithmic_bytes": att_bytes},
+                      "attention": round(att_ms, 5),
+                      "source": f"indexer and attention (+ split combine): events around one launch in "
+                                f"{SAMPLE_EVERY} in the timed region ({len(t_idx)} and {len(t_att_live)} launches); "
+                                "topk: a breakdown pass after it with events around every kernel"},
+        # the dominant kernel (the attention and its split combine, the largest
+        # share of the step): algorithmic bytes / its mean live launch time
+        "roofline": {"kernel": "attention_tc_kernel + attention_combine_kernel", "bound": "hbm",
+                     "achieved": round(att_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(att_gbs / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
+                     "traffic": measured_traffic("attention_traffic.json", name, ("attention.cu",)),
+                     "algorithmic_bytes": att_bytes, "flops": att_flops,
+                     "tensor": {"dtype": "bf16", "achieved_tflops": round(att_tflops, 1),
+                                "peak_tflops": peaks["bf16_tflops"],
+                                "frac": round(att_tflops / peaks["bf16_tflops"], 4)}},
+        "roofline_indexer": {"kernel": "indexer_tc_kernel", "bound": "hbm", "achieved": round(idx_gbs, 1),
+                             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(idx_gbs / peaks["hbm_gbs"], 4),
+                             "peak_source": peaks["source"],
+                             "traffic": measured_traffic("indexer_traffic.json", name, ("indexer.cu",)),
+                             "algorithmic_bytes": idx_bytes},
         "gpu_launches": launches,
         "clocks": clocks.summary(t0, t1),
     }
@@ -457,12 +476,26 @@ def run_e2e(args, csd, copies, runners, stream, dev, world):
                            "call": "torch H2D copies, csa_decode_step, torch D2H copies, one stream"}}
 
 
-def kernel_hash() -> str:
+def kernel_hash(files=("indexer.cu",)) -> str:
+    """Hash of a kernel's sources (with the shared headers): a recorded ncu
+    traffic figure is used only while it matches."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("indexer.cu", "common.cuh", "ptx.cuh"):
+    for f in tuple(files) + ("common.cuh", "ptx.cuh"):
         h.update(open(os.path.join(ROOT, "compressed_sparse_decode_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
+
+
+def measured_traffic(record: str, workload: str, files) -> int | None:
+    """DRAM bytes per launch from a committed ncu record under profiles/, or
+    None when there is none for this workload or the kernel changed since."""
+    p = os.path.join(ROOT, "profiles", record)
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("workload") == workload and d.get("kernel_source_hash") == kernel_hash(files):
+        return d.get("dram_bytes_per_launch")
+    return None
 
 
 # --------------------------------------------------------------------------
@@ -503,17 +536,30 @@ def _oracle_rows(h, wl, rows, threads):
 
 
 def cpu_baseline(x) -> dict:
+    """The oracle (as it stands) on the host cores: the whole step of the
+    workload (every query token: indexer, top-k, attention), one token per
+    thread on os.cpu_count() threads; plus a 1-thread timing of the two small
+    workloads (1K and 16K-32K context), whole."""
+    import synth
     cores = os.cpu_count() or 1
     wl = x.wl
     h = _oracle_host_inputs(x)
-    n = min(wl.B * wl.T, 8)
-    rows = list(range(n))
+    rows = list(range(wl.B * wl.T))
     t0 = time.time()
-    _oracle_rows(h, wl, rows, min(cores, n))
+    _oracle_rows(h, wl, rows, cores)
     dt = time.time() - t0
-    return {"value": round(n / dt, 3), "unit": UNIT, "cores": min(cores, n), "kind": "oracle",
-            "sample": f"{n} of the {wl.B * wl.T} query tokens of one decode step (indexer, top-k, attention), "
-                      f"{dt:.1f} s wall"}
+    single = {}
+    for small in ("csa_b1_ctx1k_k64", "csa_b8_ctx16k32k_k512"):
+        xs = synth.generate(small, seed=0, device="cpu")
+        hs = _oracle_host_inputs(xs)
+        n = xs.wl.B * xs.wl.T
+        ts = time.time()
+        _oracle_rows(hs, xs.wl, list(range(n)), 1)
+        single[small] = round(n / (time.time() - ts), 3)
+    return {"value": round(len(rows) / dt, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"the whole step: all {len(rows)} query tokens of the workload (indexer, top-k, attention), "
+                      f"one token per thread, {dt:.1f} s wall",
+            "single_thread_tokens_per_s": single}
 
 
 def run_reference(args, rank, world, local_rank):
@@ -548,12 +594,14 @@ def run_reference(args, rank, world, local_rank):
 
 
 def report_configs():
-    """Per-kernel times of every workload in synth.WORKLOADS (a markdown table
-    on stdout, not the benchmark's JSON line): events around each call, five
-    warm-up calls, the median of 30 timed calls over rotating input copies.
+    """Per-kernel times of every workload in synth.WORKLOADS, one JSON line
+    per workload (not the benchmark's line): events around each call, five
+    warm-up calls, the median of 30 timed calls over rotating input copies,
+    with nvidia-smi clocks sampled during each workload's timed calls.
     Roofline = max(algorithmic bytes / measured HBM peak, flops / FP8 peak),
-    with the FP8 dense peak taken as twice the measured BF16 one; the
-    attention's BF16 MMAs make the BF16 figure the tighter one for it."""
+    FP8 dense peak taken as twice the measured BF16 one (the pages' method
+    computes on FP8 data); the attention's tensor fraction is also given
+    against the BF16 peak, the precision its MMAs run in."""
     import numpy as np
     import torch
 
@@ -566,8 +614,12 @@ def report_configs():
     peaks = load_peaks()
     hbm = peaks["hbm_gbs"] * 1e9
     fp8 = 2 * peaks["bf16_tflops"] * 1e12
-    print("| workload | kernel | µs (median) | algorithmic MB | Gflop | roofline µs | fraction |")
-    print("|---|---|---|---|---|---|---|")
+    bf16 = peaks["bf16_tflops"] * 1e12
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
     for name, wl in synth.WORKLOADS.items():
         base = synth.generate(name, seed=0, device=dev)
         copies = [base] + [base.clone() for _ in range(N_COPIES - 1)]
@@ -583,12 +635,10 @@ def report_configs():
                 for r in runners:
                     r.indexer(); r.topk(); r.attention()
             torch.cuda.synchronize(dev)
-            cnt = runners[0].cnt.cpu().numpy()
-            cands = int(cnt.sum() + nswa.sum())
+            ab, af = attention_work(runners[0].cnt.cpu().numpy(), base)
             work["indexer"] = (lambda i: runners[i].indexer(), indexer_bytes(base), 16384 * float(nvis.sum()))
             work["topk"] = (lambda i: runners[i].topk(), 4 * int(nvis.sum()) + 4 * wl.B * wl.T * wl.k, 0.0)
-            work["attention"] = (lambda i: runners[i].attention(), attention_bytes(runners[0].cnt.cpu().numpy(), base),
-                                 262144.0 * cands)
+            work["attention"] = (lambda i: runners[i].attention(), ab, af)
         else:
             comps = [csd.cache_desc(x.comp, wl.ncap, x.seq_stride) for x in copies]
             outs = [(torch.empty_like(x.q), torch.empty((wl.B, wl.T, 128), dtype=torch.float32, device=dev),
@@ -600,6 +650,11 @@ def report_configs():
                                               out=o, lse=l, ws=w, stream=stream)
             cands = int(nvis.sum() + nswa.sum())
             work["hca attention"] = (hca, cands * 592 + wl.B * wl.T * (2 * 128 * 512 * 2 + 128 * 4), 262144.0 * cands)
+        kernels = {}
+        clocks = ClockSampler(uuid)
+        clocks.start()
+        time.sleep(0.3)
+        t0 = time.time()
         for kern, (fn, nbytes, flops) in work.items():
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(30)]
             with torch.cuda.stream(stream):
@@ -612,19 +667,116 @@ def report_configs():
             torch.cuda.synchronize(dev)
             us = float(np.median([a.elapsed_time(b) * 1e3 for a, b in ev]))
             roof = max(nbytes / hbm, flops / fp8) * 1e6
-            print(f"| {name} | {kern} | {us:.2f} | {nbytes / 1e6:.2f} | {flops / 1e9:.2f} | {roof:.2f} | "
-                  f"{roof / us:.2f} |", flush=True)
+            entry = {"us_median": round(us, 2), "algorithmic_mb": round(nbytes / 1e6, 3),
+                     "gflop": round(flops / 1e9, 3), "roofline_us": round(roof, 3), "frac": round(roof / us, 4),
+                     "bound": "hbm" if nbytes / hbm >= flops / fp8 else "tensor",
+                     "achieved_gbs": round(nbytes / (us / 1e6) / 1e9, 1)}
+            if "attention" in kern:
+                entry["tensor_frac_bf16"] = round(flops / bf16 * 1e6 / us, 4)
+            kernels[kern] = entry
+        t1 = time.time()
+        time.sleep(0.1)
+        clocks.stop()
         if csd.csa_read_device_error(stream):
             raise RuntimeError(f"device error word set on {name}")
+        step_us = sum(v["us_median"] for v in kernels.values())
+        print(json.dumps({"workload": name, "kind": wl.kind, "batch": wl.B, "tokens_per_seq": wl.T,
+                          "compressed_entries": wl.ncap, "topk": wl.k, "kernels": kernels,
+                          "sum_of_kernels_us": round(step_us, 2),
+                          "tokens_per_s_from_sum": round(wl.B * wl.T / (step_us / 1e6), 1),
+                          "clocks": clocks.summary(t0, t1),
+                          "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
+                                    "fp8_tflops_taken": 2 * peaks["bf16_tflops"], "source": peaks["source"]},
+                          "timing": "events around each C-ABI call (no programmatic-launch overlap), 5 warm-up "
+                                    "calls, median of 30 over 3 rotating input copies"}), flush=True)
         del copies, base, work
         torch.cuda.empty_cache()
-    print(f"\npeaks: HBM {peaks['hbm_gbs']:.0f} GB/s, BF16 {peaks['bf16_tflops']:.0f} TFLOP/s ({peaks['source']}); "
-          f"FP8 taken as 2x BF16")
+
+
+def graph_replay(args):
+    """Whole-step CUDA graph ("ROADMAP -- Stage E", section E9): LAYERS decode
+    steps, each layer with its own paged cache and block table, issued as
+    direct C-ABI calls and as one captured graph; host clock around 50
+    iterations of all layers after warm-up; the replay checked bit for bit
+    against the direct calls first."""
+    import torch
+
+    import compressed_sparse_decode_gb300 as csd
+    import synth
+    csd.build()
+    csd.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    name = args.workload or "csa_b1_ctx1k_k64"
+    layers = [synth.generate(name, seed=100 + i, device=dev, paged=True) for i in range(args.graph_replay)]
+    wl = layers[0].wl
+    comps = [csd.cache_desc(x.comp, wl.ncap, x.seq_stride, x.block_table, x.page_records) for x in layers]
+    wss = [csd.workspace(csd.OP_DECODE_STEP, wl.B, wl.T, wl.ncap, wl.k, dev) for _ in layers]
+    outs = [(torch.empty_like(x.q), torch.empty((wl.B, wl.T, 128), dtype=torch.float32, device=dev)) for x in layers]
+    stream = torch.cuda.Stream(device=dev)
+    status = csd.status_word(dev)
+    lib = csd.load()
+    p = lambda t: C.c_void_p(t.data_ptr()) if t is not None else None
+    calls = [[p(x.q_idx), p(x.q_idx_scale), p(x.w_idx), p(x.k_idx), p(x.k_idx_scale), p(x.q), p(x.sink),
+              C.c_float(SCALE), c, p(x.ring), x.ring.shape[1], wl.W, p(x.q_pos), p(x.n_comp), wl.B, wl.T, wl.ncap,
+              wl.m, wl.k, p(o), p(l), None, None, p(w), C.c_size_t(w.numel()), p(status),
+              C.c_void_p(stream.cuda_stream)] for x, c, w, (o, l) in zip(layers, comps, wss, outs)]
+
+    def direct():
+        for a in calls:
+            st = lib.csa_decode_step(*a)
+            if st:
+                raise RuntimeError(f"csa_decode_step: {csd.status_string(st)}")
+
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            direct()
+    torch.cuda.synchronize(dev)
+    want = [(o.clone(), l.clone()) for o, l in outs]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        direct()
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    if not all(torch.equal(o, wo) and torch.equal(l, wlse) for (o, l), (wo, wlse) in zip(outs, want)):
+        raise RuntimeError("graph replay differs from the direct calls")
+
+    def clock(fn, n=50):
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                fn()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for _ in range(n):
+                fn()
+        torch.cuda.synchronize(dev)
+        return (time.perf_counter() - t0) / n * 1e6
+
+    n0 = csd.csa_kernel_launches()
+    with torch.cuda.stream(stream):
+        direct()
+    launches = csd.csa_kernel_launches() - n0
+    t_direct = clock(direct)
+    t_graph = clock(graph.replay)
+    if csd.csa_read_device_error(stream):
+        raise RuntimeError("device error word set")
+    print(json.dumps({"graph_replay": {"workload": name, "layers": args.graph_replay,
+                                       "direct_us_per_step": round(t_direct, 2),
+                                       "graph_us_per_step": round(t_graph, 2),
+                                       "speedup": round(t_direct / t_graph, 3),
+                                       "launches_per_step": launches,
+                                       "clock": "host wall clock around 50 iterations of all layers",
+                                       "check": "replay bit-identical to the direct calls"}}), flush=True)
 
 
 def main():
     args = parse()
     rank, world, local_rank = dist_env()
+    if args.graph_replay:
+        if rank == 0:
+            graph_replay(args)
+        return
     if args.report_configs:
         if rank == 0:
             report_configs()
