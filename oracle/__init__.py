@@ -79,6 +79,14 @@ def _load():
             lib.oracle_hca_attention.restype = i32
             lib.oracle_gather.argtypes = cache + [P, i32, i32, P, P, P] + [i32] * 6 + [P, P]
             lib.oracle_gather.restype = i32
+            lib.oracle_e2m1_value.argtypes = [C.c_uint8]
+            lib.oracle_e2m1_value.restype = dbl
+            lib.oracle_e2m1_code.argtypes = [dbl]
+            lib.oracle_e2m1_code.restype = C.c_uint8
+            lib.oracle_e2m1_quantize.argtypes = [P, i32, i32, P, P]
+            lib.oracle_e2m1_quantize.restype = None
+            lib.oracle_inverse_rope.argtypes = [P, i32, i32, i32, dbl]
+            lib.oracle_inverse_rope.restype = None
             _lib = lib
     return _lib
 
@@ -299,3 +307,46 @@ def gather(cache: Cache, ring, W: int, topk_idx, topk_cnt, q_pos, threads: int =
                                  _ptr(kv_out), _ptr(kv_cnt)), "gather")
     _rows(B * T, threads, run)
     return kv_out, kv_cnt
+
+
+# --------------------------------------------------------------------------
+# Attention output epilogue (inverse RoPE, E2M1 output)
+# --------------------------------------------------------------------------
+
+def e2m1_value(code: int) -> float:
+    return _load().oracle_e2m1_value(code)
+
+
+def e2m1_code(v: float) -> int:
+    return int(_load().oracle_e2m1_code(float(v)))
+
+
+def e2m1_quantize(x, block: int = 128):
+    """x [..., n] (any float dtype, widened exactly to double) -> (codes
+    [..., n] uint8, one code per byte; scales [..., ceil(n/block)] float64)."""
+    lib = _load()
+    x = _np(x, np.float64)
+    n = x.shape[-1]
+    flat = x.reshape(-1, n)
+    nb = (n + block - 1) // block
+    codes = np.empty(flat.shape, dtype=np.uint8)
+    scales = np.empty((flat.shape[0], nb), dtype=np.float64)
+    for i in range(flat.shape[0]):
+        lib.oracle_e2m1_quantize(_ptr(flat[i]), n, block, _ptr(codes[i]), _ptr(scales[i]))
+    return codes.reshape(x.shape), scales.reshape(*x.shape[:-1], nb)
+
+
+def inverse_rope(o, pos, theta: float, Dn=DN, Dr=DR):
+    """o [rows, ..., Dn+Dr] float64 (a copy is rotated), pos [rows] -> the rows
+    with their rope dims turned back by RoPE(-pos)."""
+    lib = _load()
+    out = np.array(_np(o, np.float64), copy=True)
+    pos = np.asarray(pos).reshape(-1)
+    D = out.shape[-1]
+    view = out.reshape(len(pos), -1, D)
+    for r in range(len(pos)):
+        for j in range(view.shape[1]):
+            row = np.ascontiguousarray(view[r, j])
+            lib.oracle_inverse_rope(_ptr(row), Dn, Dr, int(pos[r]), float(theta))
+            view[r, j] = row
+    return out

@@ -11,12 +11,14 @@
  * Sources (web pages of the DSV4 "nvfp4-megamoe-kernel" project):
  *   [AUDIT]   "DSV4 Audit -- Decode Repetition + Precision / Tensor-Core Plan"
  *             (FINAL_STRETCH.md): section A3 (visible range, SWA overlap),
+ *             section A4 (inverse RoPE on the attention output),
  *             section B1 (FP8 nope + BF16 rope latent), section B2 (indexer).
  *   [ROADMAP] "ROADMAP -- Stage E and the path to a runnable model"
  *             (archived_plans/NEXT_PRIORITIES_PART_2.md): section E1 (gathers
  *             of selected / all compressed entries and of the SWA window,
- *             FP8 entries with an inverse scale stored alongside), section E7
- *             (top-k of indexer scores).
+ *             FP8 entries with an inverse scale stored alongside), section E6
+ *             (FP4 output of the attention with a per-128-element amax),
+ *             section E7 (top-k of indexer scores).
  *   [README]  "DSV4 Inference Kernel" (README.md): section Architecture (CSA m=4,
  *             HCA m'=128, one 512-d latent shared by all 128 heads, sink
  *             weights merging sparse and SWA attention).
@@ -508,4 +510,80 @@ int oracle_gather(const uint8_t *comp, int64_t seq_stride, const int32_t *block_
     }
     free(cand);
     return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Attention output epilogue                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* OCP FP4 E2M1 (the low 4 bits of `code`): sign bit 3, exponent bits 2..1
+ * (bias 1), mantissa bit 0; exponent 0 is subnormal (mantissa / 2). The
+ * magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6; there is no infinity or NaN.
+ * [ROADMAP] E6 names E2M1 as the format of the attention's FP4 output. */
+double oracle_e2m1_value(uint8_t code)
+{
+    int sign = (code >> 3) & 1;
+    int expo = (code >> 1) & 3;
+    int mant = code & 1;
+    double mag = expo == 0 ? (double)mant / 2.0 : ldexp(1.0 + (double)mant / 2.0, expo - 1);
+    return sign ? -mag : mag;
+}
+
+/* The E2M1 code nearest to v: among the eight magnitudes the one closest to
+ * |v|, a tie going to the code with mantissa bit 0 (round half to even);
+ * magnitudes above 6 give 6 (saturation). The sign bit is v's sign bit, so a
+ * negative value that rounds to zero gives the negative-zero code 8. */
+uint8_t oracle_e2m1_code(double v)
+{
+    double a = fabs(v) > 6.0 ? 6.0 : fabs(v), best_d = INFINITY;  /* saturation */
+    int c, best = 0;
+    for (c = 0; c < 8; ++c) {
+        double d = fabs(oracle_e2m1_value((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
+            best_d = d;
+            best = c;
+        }
+    }
+    return (uint8_t)(best | (signbit(v) ? 8 : 0));
+}
+
+/* E2M1 quantisation of x[0..n) in blocks of `block` elements (ragged last
+ * block) ([ROADMAP] E6: an E2M1 pack with a per-128-element block amax).
+ * Reading: block i's multiplier is s_i = amax_i / 6 (the largest E2M1
+ * magnitude), 1 for an all-zero block, so that x ~ e2m1 * s_i;
+ * codes[d] = the E2M1 code nearest to x[d] / s_i, one code per byte. */
+void oracle_e2m1_quantize(const double *x, int n, int block, uint8_t *codes, double *scales)
+{
+    int b0, d;
+    for (b0 = 0; b0 < n; b0 += block) {
+        int b1 = b0 + block < n ? b0 + block : n;
+        double amax = 0.0, s;
+        for (d = b0; d < b1; ++d)
+            if (fabs(x[d]) > amax)
+                amax = fabs(x[d]);
+        s = amax > 0.0 ? amax / 6.0 : 1.0;
+        scales[b0 / block] = s;
+        for (d = b0; d < b1; ++d)
+            codes[d] = oracle_e2m1_code(x[d] / s);
+    }
+}
+
+/* Inverse RoPE on one attention output row o[0..Dn+Dr) ([AUDIT] A4: the
+ * output is rotated by RoPE(-t) at the query position t, turning the absolute
+ * positions carried by the summed latents into relative ones). Reading (the
+ * pages give no convention): the rope dims are [Dn, Dn+Dr); pair i is
+ * (Dn+2i, Dn+2i+1) and turns by t * theta^(-2i/Dr) radians at position t;
+ * the inverse turns it back by the same angle:
+ *   x' = x cos(a) + y sin(a),  y' = -x sin(a) + y cos(a),  a = t theta^(-2i/Dr).
+ * The nope dims are left as they are. */
+void oracle_inverse_rope(double *o, int Dn, int Dr, int pos, double theta)
+{
+    int i;
+    for (i = 0; i < Dr / 2; ++i) {
+        double a = (double)pos * pow(theta, -2.0 * (double)i / (double)Dr);
+        double c = cos(a), s = sin(a);
+        double x = o[Dn + 2 * i], y = o[Dn + 2 * i + 1];
+        o[Dn + 2 * i] = x * c + y * s;
+        o[Dn + 2 * i + 1] = -x * s + y * c;
+    }
 }

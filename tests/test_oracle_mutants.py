@@ -10,7 +10,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "csa_oracle.c")
 PINS = ["tests/test_oracle_formats.py", "tests/test_oracle_visibility.py", "tests/test_oracle_indexer.py",
-        "tests/test_oracle_topk.py", "tests/test_oracle_attention.py"]
+        "tests/test_oracle_topk.py", "tests/test_oracle_attention.py", "tests/test_oracle_epilogue.py"]
 
 MUTANTS = {
     "relu_dropped": ("acc += (double)w[h] * (dot > 0.0 ? dot : 0.0);", "acc += (double)w[h] * dot;"),
@@ -36,6 +36,11 @@ MUTANTS = {
     "page_index_wrong": ("int page = c / page_records;", "int page = c % page_records;"),
     "seq_stride_ignored": ("rec = (int64_t)b * seq_stride + c;", "rec = (int64_t)b + c;"),
     "selected_list_truncated": ("for (i = 0; i < cnt; ++i) {\n        const uint8_t *rec", "for (i = 1; i < cnt; ++i) {\n        const uint8_t *rec"),
+    "e2m1_bias_0": ("ldexp(1.0 + (double)mant / 2.0, expo - 1)", "ldexp(1.0 + (double)mant / 2.0, expo)"),
+    "e2m1_ties_to_odd": ("(c & 1) == 0 && (best & 1) == 1", "(c & 1) == 1 && (best & 1) == 0"),
+    "e2m1_scale_amax_over_4": ("s = amax > 0.0 ? amax / 6.0 : 1.0;", "s = amax > 0.0 ? amax / 4.0 : 1.0;"),
+    "inverse_rope_turns_forward": ("double c = cos(a), s = sin(a);", "double c = cos(a), s = -sin(a);"),
+    "rope_frequency_exponent": ("pow(theta, -2.0 * (double)i / (double)Dr)", "pow(theta, -(double)i / (double)Dr)"),
     "value_uses_query_not_latent": ("acc += exp(z[j] - M) * x[(size_t)j * D + d];", "acc += exp(z[j] - M) * qd[d];"),
 }
 
