@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--report-configs", action="store_true",
                     help="print one JSON line of per-kernel times for every workload instead of the benchmark line")
+    ap.add_argument("--prefill", type=int, default=0, metavar="T",
+                    help="time T tokens of one 128K sequence as one step against T single-token steps")
     ap.add_argument("--graph-replay", type=int, default=0, metavar="LAYERS",
                     help="time LAYERS decode steps (one per layer, each with its own paged cache) as direct calls "
                          "and as one replayed CUDA graph, on --workload (default: the 1K-context one)")
@@ -770,9 +772,76 @@ def graph_replay(args):
                                        "check": "replay bit-identical to the direct calls"}}), flush=True)
 
 
+def prefill(args):
+    """Many query tokens per sequence in one step ("ROADMAP -- Stage E",
+    section E8: prefill spread over many CTAs): T consecutive tokens of one
+    128K-context sequence (top-2048) as one csa_decode_step over B*T rows,
+    against the same tokens issued as T single-token steps (one query row per
+    launch). Device time with CUDA events on the calling stream, median of 20
+    after 3 warm-ups."""
+    import torch
+
+    import compressed_sparse_decode_gb300 as csd
+    import synth
+    csd.build()
+    csd.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    T = args.prefill
+    wl = synth.custom("csa", B=1, T=T, ncap=32768, k=2048, ctx=131072, name=f"csa_b1_t{T}_ctx128k_k2048")
+    x = synth.generate(wl, seed=0, device=dev)
+    comp = csd.cache_desc(x.comp, wl.ncap, x.seq_stride)
+    out = torch.empty_like(x.q)
+    lse = torch.empty((1, T, 128), dtype=torch.float32, device=dev)
+    ws = csd.workspace(csd.OP_DECODE_STEP, 1, T, wl.ncap, wl.k, dev)
+    ws1 = csd.workspace(csd.OP_DECODE_STEP, 1, 1, wl.ncap, wl.k, dev)
+    one = [(x.q_idx[:, t:t + 1].contiguous(), x.q_idx_scale[:, t:t + 1].contiguous(), x.w_idx[:, t:t + 1].contiguous(),
+            x.q[:, t:t + 1].contiguous(), x.q_pos[:, t:t + 1].contiguous(), torch.empty_like(x.q[:, t:t + 1]),
+            torch.empty((1, 1, 128), dtype=torch.float32, device=dev)) for t in range(T)]
+
+    def batched():
+        csd.csa_decode_step(x.q_idx, x.q_idx_scale, x.w_idx, x.k_idx, x.k_idx_scale, x.q, x.sink, SCALE, comp, x.ring,
+                            wl.W, x.q_pos, x.n_comp, wl.m, wl.k, out=out, lse=lse, ws=ws)
+
+    def token_loop():
+        for qi, qs, wi, q, qp, o, l in one:
+            csd.csa_decode_step(qi, qs, wi, x.k_idx, x.k_idx_scale, q, x.sink, SCALE, comp, x.ring, wl.W, qp, x.n_comp,
+                                wl.m, wl.k, out=o, lse=l, ws=ws1)
+
+    def timed(fn, n=20):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(n):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b) * 1e3)
+        return float(statistics.median(ts))
+
+    t_b, t_l = timed(batched), timed(token_loop)
+    if csd.csa_read_device_error():
+        raise RuntimeError("device error word set")
+    # the batched step's rows agree with the single-token steps' rows
+    cos = min(float(torch.nn.functional.cosine_similarity(out[0, t].float(), one[t][5][0, 0].float(), dim=-1).min())
+              for t in range(T))
+    print(json.dumps({"prefill": {"workload": wl.name, "tokens": T, "batched_us": round(t_b, 2),
+                                  "token_loop_us": round(t_l, 2), "speedup": round(t_l / t_b, 2),
+                                  "batched_tokens_per_s": round(T / t_b * 1e6, 1),
+                                  "min_cos_batched_vs_loop": round(cos, 6),
+                                  "clock": "CUDA events, median of 20 after 3 warm-ups"}}), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local_rank = dist_env()
+    if args.prefill:
+        if rank == 0:
+            prefill(args)
+        return
     if args.graph_replay:
         if rank == 0:
             graph_replay(args)

@@ -21,7 +21,7 @@ from ._build import LIB, build  # noqa: F401  (build() compiles libcsa.so in-tre
 
 HEADS, DIM, NOPE, ROPE, SCALE_BLOCK, RECORD_BYTES = 128, 512, 448, 64, 128, 592
 IDX_HEADS, IDX_DIM = 64, 128
-MAX_TOKENS_PER_SEQ, MAX_TOPK, MAX_SWA_WINDOW = 4, 2048, 512
+MAX_TOKENS_PER_SEQ, MAX_TOPK, MAX_SWA_WINDOW = 128, 2048, 512
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_BAD_INDEX = range(7)
 OP_INDEXER, OP_TOPK, OP_ATTENTION, OP_HCA_ATTENTION, OP_DECODE_STEP = range(5)
@@ -31,7 +31,8 @@ EXPORTED = ["csa_workspace_bytes", "csa_indexer_logits", "csa_topk", "csa_gather
             "csa_check_device_status", "csa_read_device_error", "csa_debug_set_wait_limit_ns",
             "csa_status_string", "csa_version", "csa_kernel_launches",
             "csa_sink_attention_decode_noalloc", "csa_pipeline_staging_bytes", "csa_pipeline_create",
-            "csa_decode_step_host", "csa_pipeline_wait", "csa_pipeline_sync", "csa_pipeline_destroy"]
+            "csa_decode_step_host", "csa_pipeline_wait", "csa_pipeline_sync", "csa_pipeline_destroy",
+            "csa_sink_attention_decode_ex", "hca_sink_attention_decode_ex"]
 PIPELINE_MAX_DEPTH = 4
 
 
@@ -45,6 +46,11 @@ class csa_cache_desc(C.Structure):
     _fields_ = [("base", C.c_void_p), ("n_records", C.c_int64), ("seq_stride", C.c_int64),
                 ("block_table", C.c_void_p), ("page_records", C.c_int32), ("max_pages", C.c_int32),
                 ("seq_capacity", C.c_int32)]
+
+
+class csa_attention_epilogue(C.Structure):
+    _fields_ = [("inverse_rope", C.c_int32), ("rope_theta", C.c_float), ("out_fp4", C.c_void_p),
+                ("out_fp4_scale", C.c_void_p)]
 
 
 _lib = None
@@ -87,6 +93,13 @@ def load(path: str | None = None):
         lib.csa_sink_attention_decode_noalloc.argtypes = ([P, P, f32, csa_cache_desc, P, i32, i32, P, P, P, i32, i32,
                                                            i32, P, P, P, P])
         lib.csa_sink_attention_decode_noalloc.restype = st
+        EP = C.POINTER(csa_attention_epilogue)
+        lib.csa_sink_attention_decode_ex.argtypes = ([P, P, f32, csa_cache_desc, P, i32, i32, P, P, P, i32, i32, i32,
+                                                      P, P, EP, P, sz, P, P])
+        lib.csa_sink_attention_decode_ex.restype = st
+        lib.hca_sink_attention_decode_ex.argtypes = ([P, P, f32, csa_cache_desc, P, P, i32, i32, P, i32, i32, i32,
+                                                      P, P, EP, P, sz, P, P])
+        lib.hca_sink_attention_decode_ex.restype = st
         lib.csa_pipeline_staging_bytes.argtypes = [i32, i32, i32]
         lib.csa_pipeline_staging_bytes.restype = sz
         lib.csa_pipeline_create.argtypes = [C.POINTER(C.c_void_p), i32, i32, i32, P, sz, P]
@@ -265,27 +278,51 @@ def csa_gather_swa(comp: csa_cache_desc, swa_ring, W: int, topk_idx, topk_cnt, q
     return kv_out, kv_cnt
 
 
+def _epilogue(B: int, T: int, dev, inverse_rope: bool, rope_theta: float, fp4_out: bool, out_fp4, out_fp4_scale):
+    """The output-epilogue struct (None when neither step is asked for) and
+    the E2M1 output tensors."""
+    if not inverse_rope and not fp4_out:
+        return None, None, None
+    if fp4_out:
+        if out_fp4 is None:
+            out_fp4 = torch.empty((B, T, HEADS, DIM // 2), dtype=torch.uint8, device=dev)
+        if out_fp4_scale is None:
+            out_fp4_scale = torch.empty((B, T, HEADS, DIM // SCALE_BLOCK), dtype=torch.float32, device=dev)
+    epi = csa_attention_epilogue(1 if inverse_rope else 0, float(rope_theta),
+                                 _ptr(out_fp4, "out_fp4", torch.uint8, (B, T, HEADS, DIM // 2)) if fp4_out else None,
+                                 _ptr(out_fp4_scale, "out_fp4_scale", torch.float32,
+                                      (B, T, HEADS, DIM // SCALE_BLOCK)) if fp4_out else None)
+    return epi, out_fp4, out_fp4_scale
+
+
 def csa_sink_attention_decode(q, sink, softmax_scale: float, comp: csa_cache_desc, swa_ring, W: int, topk_idx,
-                              topk_cnt, q_pos, out=None, lse=None, ws=None, stream=None, status=None):
+                              topk_cnt, q_pos, out=None, lse=None, ws=None, stream=None, status=None,
+                              inverse_rope: bool = False, rope_theta: float = 10000.0, fp4_out: bool = False,
+                              out_fp4=None, out_fp4_scale=None):
+    """Returns (out, lse); with fp4_out, ((out_fp4, out_fp4_scale), lse).
+    inverse_rope / fp4_out select the output epilogue (csa_attention_epilogue)."""
     B, T = q_pos.shape
     k = topk_idx.shape[2]
     R = swa_ring.shape[1]
     dev = q.device
-    if out is None:
+    epi, out_fp4, out_fp4_scale = _epilogue(B, T, dev, inverse_rope, rope_theta, fp4_out, out_fp4, out_fp4_scale)
+    if out is None and not fp4_out:
         out = torch.empty((B, T, HEADS, DIM), dtype=torch.bfloat16, device=dev)
     if lse is None:
         lse = torch.empty((B, T, HEADS), dtype=torch.float32, device=dev)
     if ws is None:
         ws = workspace(OP_ATTENTION, B, T, comp.seq_capacity, k, dev)
-    _check(load().csa_sink_attention_decode(
-        _ptr(q, "q", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(sink, "sink", torch.float32, (HEADS,)),
-        float(softmax_scale), comp, _ptr(swa_ring, "swa_ring", torch.uint8, (B, R, RECORD_BYTES)), R, int(W),
-        _ptr(topk_idx, "topk_idx", torch.int32, (B, T, k)), _ptr(topk_cnt, "topk_cnt", torch.int32, (B, T)),
-        _ptr(q_pos, "q_pos", torch.int32, (B, T)), B, T, k,
-        _ptr(out, "out", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(lse, "lse", torch.float32, (B, T, HEADS)),
-        _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _status(status, dev), _stream(stream)),
-        "csa_sink_attention_decode")
-    return out, lse
+    args = [_ptr(q, "q", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(sink, "sink", torch.float32, (HEADS,)),
+            float(softmax_scale), comp, _ptr(swa_ring, "swa_ring", torch.uint8, (B, R, RECORD_BYTES)), R, int(W),
+            _ptr(topk_idx, "topk_idx", torch.int32, (B, T, k)), _ptr(topk_cnt, "topk_cnt", torch.int32, (B, T)),
+            _ptr(q_pos, "q_pos", torch.int32, (B, T)), B, T, k,
+            _ptr(out, "out", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(lse, "lse", torch.float32, (B, T, HEADS))]
+    tail = [_ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _status(status, dev), _stream(stream)]
+    if epi is None:
+        _check(load().csa_sink_attention_decode(*args, *tail), "csa_sink_attention_decode")
+    else:
+        _check(load().csa_sink_attention_decode_ex(*args, C.byref(epi), *tail), "csa_sink_attention_decode_ex")
+    return ((out_fp4, out_fp4_scale) if fp4_out else out), lse
 
 
 def csa_sink_attention_decode_noalloc(q, sink, softmax_scale: float, comp: csa_cache_desc, swa_ring, W: int, topk_idx,
@@ -312,25 +349,31 @@ def csa_sink_attention_decode_noalloc(q, sink, softmax_scale: float, comp: csa_c
 
 
 def hca_sink_attention_decode(q, sink, softmax_scale: float, comp: csa_cache_desc, n_comp, swa_ring, W: int, q_pos,
-                              m_hca: int = 128, out=None, lse=None, ws=None, stream=None, status=None):
+                              m_hca: int = 128, out=None, lse=None, ws=None, stream=None, status=None,
+                              inverse_rope: bool = False, rope_theta: float = 10000.0, fp4_out: bool = False,
+                              out_fp4=None, out_fp4_scale=None):
+    """Returns (out, lse); with fp4_out, ((out_fp4, out_fp4_scale), lse)."""
     B, T = q_pos.shape
     R = swa_ring.shape[1]
     dev = q.device
-    if out is None:
+    epi, out_fp4, out_fp4_scale = _epilogue(B, T, dev, inverse_rope, rope_theta, fp4_out, out_fp4, out_fp4_scale)
+    if out is None and not fp4_out:
         out = torch.empty((B, T, HEADS, DIM), dtype=torch.bfloat16, device=dev)
     if lse is None:
         lse = torch.empty((B, T, HEADS), dtype=torch.float32, device=dev)
     if ws is None:
         ws = workspace(OP_HCA_ATTENTION, B, T, comp.seq_capacity, 0, dev)
-    _check(load().hca_sink_attention_decode(
-        _ptr(q, "q", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(sink, "sink", torch.float32, (HEADS,)),
-        float(softmax_scale), comp, _ptr(n_comp, "n_comp", torch.int32, (B,)),
-        _ptr(swa_ring, "swa_ring", torch.uint8, (B, R, RECORD_BYTES)), R, int(W),
-        _ptr(q_pos, "q_pos", torch.int32, (B, T)), B, T, int(m_hca),
-        _ptr(out, "out", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(lse, "lse", torch.float32, (B, T, HEADS)),
-        _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _status(status, dev), _stream(stream)),
-        "hca_sink_attention_decode")
-    return out, lse
+    args = [_ptr(q, "q", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(sink, "sink", torch.float32, (HEADS,)),
+            float(softmax_scale), comp, _ptr(n_comp, "n_comp", torch.int32, (B,)),
+            _ptr(swa_ring, "swa_ring", torch.uint8, (B, R, RECORD_BYTES)), R, int(W),
+            _ptr(q_pos, "q_pos", torch.int32, (B, T)), B, T, int(m_hca),
+            _ptr(out, "out", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(lse, "lse", torch.float32, (B, T, HEADS))]
+    tail = [_ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _status(status, dev), _stream(stream)]
+    if epi is None:
+        _check(load().hca_sink_attention_decode(*args, *tail), "hca_sink_attention_decode")
+    else:
+        _check(load().hca_sink_attention_decode_ex(*args, C.byref(epi), *tail), "hca_sink_attention_decode_ex")
+    return ((out_fp4, out_fp4_scale) if fp4_out else out), lse
 
 
 def csa_decode_step(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q, sink, softmax_scale: float,

@@ -3,6 +3,7 @@
 // synchronises the device (except csa_read_device_error, a diagnostic).
 // In-kernel problems go to the caller's status word (an int32 in device
 // memory passed to every compute call).
+#include <cmath>
 #include <cstdint>
 #include <atomic>
 #include <cstring>
@@ -21,7 +22,8 @@ cudaError_t launch_gather(const csa_cache_desc &, const void *, int, int, const 
 size_t attention_workspace_bytes(int B, int T, int max_selected, int W);
 cudaError_t launch_attention(const void *, const float *, float, const csa_cache_desc &, const void *, int, int,
                              const int32_t *, const int32_t *, const int32_t *, int, const int32_t *, int, int, int,
-                             bool, void *, float *, void *, size_t, int *, cudaStream_t);
+                             bool, void *, float *, const csa_attention_epilogue *, void *, size_t, int *,
+                             cudaStream_t);
 }  // namespace csa
 
 namespace csa {
@@ -224,29 +226,60 @@ csa_status_t csa_gather_swa(csa_cache_desc comp, const void *swa_ring, int R, in
                                      status, stream));
 }
 
-csa_status_t csa_sink_attention_decode(const void *q, const float *sink, float softmax_scale, csa_cache_desc comp,
-                                       const void *swa_ring, int R, int W, const int32_t *topk_idx,
-                                       const int32_t *topk_cnt, const int32_t *q_pos, int B, int T, int k, void *out,
-                                       float *lse, void *workspace, size_t workspace_bytes, int32_t *status,
-                                       cudaStream_t stream) {
-    const csa_status_t a = attention_arg_status(q, sink, softmax_scale, comp, swa_ring, R, W, topk_idx, topk_cnt,
-                                                q_pos, B, T, k, out, lse, status);
+namespace {
+// An epilogue the kernels can apply; `out` is required unless the output is E2M1.
+csa_status_t epilogue_status(const csa_attention_epilogue *epi, const void *out) {
+    const bool fp4 = epi && epi->out_fp4;
+    if (!fp4 && (!out || !aligned16(out))) return CSA_ERR_INVALID_ARG;
+    if (!epi) return CSA_OK;
+    if (epi->inverse_rope && !(epi->rope_theta > 1.f && std::isfinite(epi->rope_theta))) return CSA_ERR_INVALID_ARG;
+    if (fp4 && (!epi->out_fp4_scale || !aligned16(epi->out_fp4) || !aligned16(epi->out_fp4_scale)))
+        return CSA_ERR_INVALID_ARG;
+    return CSA_OK;
+}
+// The output pointer the shared checks look at: E2M1 output stands in for `out`.
+const void *checked_out(const csa_attention_epilogue *epi, const void *out) {
+    return (epi && epi->out_fp4) ? static_cast<const void *>(epi->out_fp4) : out;
+}
+}  // namespace
+
+csa_status_t csa_sink_attention_decode_ex(const void *q, const float *sink, float softmax_scale, csa_cache_desc comp,
+                                          const void *swa_ring, int R, int W, const int32_t *topk_idx,
+                                          const int32_t *topk_cnt, const int32_t *q_pos, int B, int T, int k,
+                                          void *out, float *lse, const csa_attention_epilogue *epilogue,
+                                          void *workspace, size_t workspace_bytes, int32_t *status,
+                                          cudaStream_t stream) {
+    csa_status_t a = epilogue_status(epilogue, out);
+    if (a != CSA_OK) return a;
+    a = attention_arg_status(q, sink, softmax_scale, comp, swa_ring, R, W, topk_idx, topk_cnt, q_pos, B, T, k,
+                             checked_out(epilogue, out), lse, status);
     if (a != CSA_OK) return a;
     const size_t need = attention_workspace_bytes(B, T, k, W);
     if (need && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign)))
         return CSA_ERR_WORKSPACE;
     return cuda_status(launch_attention(q, sink, softmax_scale, comp, swa_ring, R, W, topk_idx, topk_cnt, nullptr, 1,
-                                        q_pos, B, T, k, false, out, lse, workspace, workspace_bytes, status, stream));
+                                        q_pos, B, T, k, false, out, lse, epilogue, workspace, workspace_bytes, status,
+                                        stream));
 }
 
-csa_status_t hca_sink_attention_decode(const void *q, const float *sink, float softmax_scale, csa_cache_desc comp,
-                                       const int32_t *n_comp, const void *swa_ring, int R, int W,
-                                       const int32_t *q_pos, int B, int T, int m_hca, void *out, float *lse,
-                                       void *workspace, size_t workspace_bytes, int32_t *status,
+csa_status_t csa_sink_attention_decode(const void *q, const float *sink, float softmax_scale, csa_cache_desc comp,
+                                       const void *swa_ring, int R, int W, const int32_t *topk_idx,
+                                       const int32_t *topk_cnt, const int32_t *q_pos, int B, int T, int k, void *out,
+                                       float *lse, void *workspace, size_t workspace_bytes, int32_t *status,
                                        cudaStream_t stream) {
-    if (!q || !sink || !n_comp || !swa_ring || !q_pos || !out || !lse) return CSA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(swa_ring) || !aligned16(out) || !valid_cache(comp, B) ||
-        !valid_status_word(status))
+    return csa_sink_attention_decode_ex(q, sink, softmax_scale, comp, swa_ring, R, W, topk_idx, topk_cnt, q_pos, B, T,
+                                        k, out, lse, nullptr, workspace, workspace_bytes, status, stream);
+}
+
+csa_status_t hca_sink_attention_decode_ex(const void *q, const float *sink, float softmax_scale, csa_cache_desc comp,
+                                          const int32_t *n_comp, const void *swa_ring, int R, int W,
+                                          const int32_t *q_pos, int B, int T, int m_hca, void *out, float *lse,
+                                          const csa_attention_epilogue *epilogue, void *workspace,
+                                          size_t workspace_bytes, int32_t *status, cudaStream_t stream) {
+    const csa_status_t a = epilogue_status(epilogue, out);
+    if (a != CSA_OK) return a;
+    if (!q || !sink || !n_comp || !swa_ring || !q_pos || !lse) return CSA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(swa_ring) || !valid_cache(comp, B) || !valid_status_word(status))
         return CSA_ERR_INVALID_ARG;
     if (!valid_dims(B, T) || W < 1 || W > CSA_MAX_SWA_WINDOW || R < W || m_hca < 1 || !(softmax_scale > 0.f))
         return CSA_ERR_INVALID_ARG;
@@ -254,8 +287,17 @@ csa_status_t hca_sink_attention_decode(const void *q, const float *sink, float s
     if (need && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign)))
         return CSA_ERR_WORKSPACE;
     return cuda_status(launch_attention(q, sink, softmax_scale, comp, swa_ring, R, W, nullptr, nullptr, n_comp, m_hca,
-                                        q_pos, B, T, comp.seq_capacity, true, out, lse, workspace, workspace_bytes,
-                                        status, stream));
+                                        q_pos, B, T, comp.seq_capacity, true, out, lse, epilogue, workspace,
+                                        workspace_bytes, status, stream));
+}
+
+csa_status_t hca_sink_attention_decode(const void *q, const float *sink, float softmax_scale, csa_cache_desc comp,
+                                       const int32_t *n_comp, const void *swa_ring, int R, int W,
+                                       const int32_t *q_pos, int B, int T, int m_hca, void *out, float *lse,
+                                       void *workspace, size_t workspace_bytes, int32_t *status,
+                                       cudaStream_t stream) {
+    return hca_sink_attention_decode_ex(q, sink, softmax_scale, comp, n_comp, swa_ring, R, W, q_pos, B, T, m_hca, out,
+                                        lse, nullptr, workspace, workspace_bytes, status, stream);
 }
 
 csa_status_t csa_decode_step(const uint8_t *q_idx, const float *q_idx_scale, const float *w_idx,

@@ -42,6 +42,8 @@
 #include <mutex>
 #include <type_traits>
 
+#include <cmath>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -51,6 +53,8 @@ namespace {
 
 constexpr int kChunk = 64;                  // candidates per chunk
 constexpr int kHalf = 256;                  // output latent dims per CTA
+constexpr int kRopePairs = 32;              // rope dims 448..511 as (x, y) pairs
+constexpr int kFp4RowBytes = kDim / 2;      // E2M1 output bytes per head
 constexpr int kQTmemDims = 384;             // Q dims held in TMEM; the rest in shared memory
 constexpr int kPtrRing = 8;                 // chunks of resolved record pointers
 constexpr int kIdxAhead = 4;                // chunks ahead whose candidate indices the producer has loaded
@@ -108,6 +112,16 @@ struct AttSmem {
 
 static_assert(sizeof(AttSmem) + 1024 <= 232448, "shared memory plan exceeds the per-CTA limit");
 
+// Output epilogue: inverse RoPE of the rope dims at the query position and/or
+// E2M1 output with one multiplier per 128 dims. Applied where the final
+// output is formed: the attention kernel with one split, else the combine.
+struct EpiParams {
+    uint8_t *out_fp4;      // null: BF16 output
+    float *out_fp4_scale;  // [rows, 128, 4]
+    int inv_rope;
+    double rope_freq[kRopePairs];  // radians per position of rope pair i
+};
+
 struct AttParams {
     const __nv_bfloat16 *q;
     const float *sink;
@@ -123,6 +137,7 @@ struct AttParams {
     float2 *part_ml;        // [rows, n_split, 128] (max, sum) in log2 units
     int *err;
     uint64_t wait_ns;  // limit of each bounded wait (drains keep kDrainWaitNs)
+    EpiParams epi;
 };
 
 struct Unit {
@@ -638,45 +653,111 @@ attention_tc_kernel(const AttParams P) {
             } else {
                 factor = l > 0.f ? 1.f / l : 0.f;
             }
-            // O half -> BF16 rows staged in shared memory (the own X buffers are
-            // free once every PV is done), then each warp writes its 32 head
-            // rows as whole 512-byte rows (one coalesced store per row). Chunk c
-            // (16 B) of row h sits at position c ^ (h & 7): conflict-free both ways.
-            uint8_t *ostage = &s.x_own[0][0];
-            uint8_t *srow = ostage + h * (kHalf * 2);
-#pragma unroll 1
-            for (int piece = 0; piece < kHalf / 32; ++piece) {
-                uint32_t o[32];
+            // With one split this CTA forms the final output of its half, and
+            // the epilogue (inverse RoPE on the rope dims, which all sit in the
+            // high half; E2M1 output) applies here; with several the combine
+            // applies it.
+            const bool final_out = P.n_split == 1;
+            const bool rope_here = final_out && P.epi.inv_rope && rank == 1;
+            float2 cs = make_float2(1.f, 0.f);  // lane i: cos, sin of rope pair i
+            if (rope_here) cs = rope_cos_sin(u.p, P.epi.rope_freq[lane]);
+            // piece p (32 dims) of this head's O half, normalised and turned back
+            auto piece_values = [&](int piece, float (&v)[32]) {
                 if (u.n_chunks > 0) {
+                    uint32_t o[32];
                     ptx::tmem_ld32(lane_base + kColO + piece * 32, o);
                     ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(o[i]) * factor;
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
                 }
+                if (rope_here && piece >= (kNope - kHalf) / 32) {  // latent dims 448..511
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const int c = piece * 4 + v;
-                    *reinterpret_cast<uint4 *>(srow + ((c ^ (h & 7)) << 4)) =
-                        make_uint4(bf16x2_bits(__uint_as_float(o[8 * v + 0]) * factor, __uint_as_float(o[8 * v + 1]) * factor),
-                                   bf16x2_bits(__uint_as_float(o[8 * v + 2]) * factor, __uint_as_float(o[8 * v + 3]) * factor),
-                                   bf16x2_bits(__uint_as_float(o[8 * v + 4]) * factor, __uint_as_float(o[8 * v + 5]) * factor),
-                                   bf16x2_bits(__uint_as_float(o[8 * v + 6]) * factor, __uint_as_float(o[8 * v + 7]) * factor));
+                    for (int e = 0; e < 16; ++e) {
+                        const int pair = (piece - (kNope - kHalf) / 32) * 16 + e;
+                        const float c = __shfl_sync(0xffffffffu, cs.x, pair);
+                        const float sn = __shfl_sync(0xffffffffu, cs.y, pair);
+                        const float x = v[2 * e], y = v[2 * e + 1];
+                        v[2 * e] = fmaf(x, c, y * sn);
+                        v[2 * e + 1] = fmaf(-x, sn, y * c);
+                    }
                 }
-            }
-            __syncwarp();
-            const uint64_t part_policy = ptx::l2_policy_evict_first();
-            __nv_bfloat16 *dst0 = (P.n_split == 1)
-                                      ? P.out + (size_t)r * kHeads * kDim + rank * kHalf
-                                      : P.part_o + ((size_t)r * P.n_split + u.split) * kHeads * kDim + rank * kHalf;
+            };
+            // Rows are staged in shared memory (the own X buffers are free once
+            // every PV is done), then each warp writes its 32 head rows whole
+            // (coalesced). Chunk c (16 B) of row h sits at position c ^ (h & 7):
+            // conflict-free both ways.
+            uint8_t *ostage = &s.x_own[0][0];
+            if (!(final_out && P.epi.out_fp4)) {
+                // BF16: 512 B per head row
+                uint8_t *srow = ostage + h * (kHalf * 2);
+#pragma unroll 1
+                for (int piece = 0; piece < kHalf / 32; ++piece) {
+                    float v[32];
+                    piece_values(piece, v);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int c = piece * 4 + q4;
+                        *reinterpret_cast<uint4 *>(srow + ((c ^ (h & 7)) << 4)) =
+                            make_uint4(bf16x2_bits(v[8 * q4 + 0], v[8 * q4 + 1]), bf16x2_bits(v[8 * q4 + 2], v[8 * q4 + 3]),
+                                       bf16x2_bits(v[8 * q4 + 4], v[8 * q4 + 5]), bf16x2_bits(v[8 * q4 + 6], v[8 * q4 + 7]));
+                    }
+                }
+                __syncwarp();
+                const uint64_t part_policy = ptx::l2_policy_evict_first();
+                __nv_bfloat16 *dst0 = final_out
+                                          ? P.out + (size_t)r * kHeads * kDim + rank * kHalf
+                                          : P.part_o + ((size_t)r * P.n_split + u.split) * kHeads * kDim + rank * kHalf;
 #pragma unroll 4
-            for (int i = 0; i < 32; ++i) {
-                const int hr = quarter * 32 + i;  // a head row of this warp
-                const uint4 v = *reinterpret_cast<const uint4 *>(ostage + hr * (kHalf * 2) + ((lane ^ (hr & 7)) << 4));
-                if (P.n_split == 1)
-                    reinterpret_cast<uint4 *>(dst0 + (size_t)hr * kDim)[lane] = v;
-                else  // split partials are read once, by the combine: evict-first
-                    ptx::stg_v4_policy(reinterpret_cast<uint4 *>(dst0 + (size_t)hr * kDim) + lane, v, part_policy);
+                for (int i = 0; i < 32; ++i) {
+                    const int hr = quarter * 32 + i;  // a head row of this warp
+                    const uint4 v = *reinterpret_cast<const uint4 *>(ostage + hr * (kHalf * 2) + ((lane ^ (hr & 7)) << 4));
+                    if (final_out)
+                        reinterpret_cast<uint4 *>(dst0 + (size_t)hr * kDim)[lane] = v;
+                    else  // split partials are read once, by the combine: evict-first
+                        ptx::stg_v4_policy(reinterpret_cast<uint4 *>(dst0 + (size_t)hr * kDim) + lane, v, part_policy);
+                }
+            } else {
+                // E2M1: two 128-dim blocks per half, each scaled by its amax / 6
+                // (a first pass over TMEM finds the amax); 128 B per head row
+                uint8_t *frow = ostage + h * (kFp4RowBytes / 2);
+#pragma unroll 1
+                for (int bl = 0; bl < 2; ++bl) {
+                    float amax = 0.f;
+#pragma unroll 1
+                    for (int pp = 0; pp < 4; ++pp) {
+                        float v[32];
+                        piece_values(4 * bl + pp, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+                    }
+                    const float sc = amax > 0.f ? amax / 6.f : 1.f;
+#pragma unroll 1
+                    for (int pp = 0; pp < 4; ++pp) {
+                        float v[32];
+                        piece_values(4 * bl + pp, v);
+                        uint32_t w[4];
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            w[q4] = e2m1x4(v[8 * q4] / sc, v[8 * q4 + 1] / sc, v[8 * q4 + 2] / sc, v[8 * q4 + 3] / sc) |
+                                    (e2m1x4(v[8 * q4 + 4] / sc, v[8 * q4 + 5] / sc, v[8 * q4 + 6] / sc,
+                                            v[8 * q4 + 7] / sc) << 16);
+                        const int c = 4 * bl + pp;
+                        *reinterpret_cast<uint4 *>(frow + ((c ^ (h & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    P.epi.out_fp4_scale[((size_t)r * kHeads + h) * 4 + rank * 2 + bl] = sc;
+                }
+                __syncwarp();
+#pragma unroll 2
+                for (int i = 0; i < 8; ++i) {
+                    const int hr = quarter * 32 + i * 4 + (lane >> 3);  // 8 lanes per 128-byte row
+                    const int c = lane & 7;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(ostage + hr * (kFp4RowBytes / 2) + ((c ^ (hr & 7)) << 4));
+                    reinterpret_cast<uint4 *>(P.epi.out_fp4 + ((size_t)r * kHeads + hr) * kFp4RowBytes +
+                                              rank * (kFp4RowBytes / 2))[c] = v;
+                }
             }
             if (rank == 0) {
                 if (P.n_split == 1)
@@ -702,10 +783,12 @@ constexpr int kCombineBatch = 8;
 __global__ void __launch_bounds__(256)
 attention_combine_kernel(const __nv_bfloat16 *__restrict__ part_o, const float2 *__restrict__ part_ml,
                          const float *__restrict__ sink, int n_split, __nv_bfloat16 *__restrict__ out,
-                         float *__restrict__ lse) {
+                         float *__restrict__ lse, const int32_t *__restrict__ q_pos, const EpiParams epi) {
     ptx::griddep_wait();  // the split partials (previous kernel in the stream) are complete
     const int r = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float2 cs = make_float2(1.f, 0.f);  // lane i: cos, sin of rope pair i
+    if (epi.inv_rope) cs = rope_cos_sin(__ldg(q_pos + r), epi.rope_freq[lane]);
     const int h = blockIdx.x * 8 + warp;
     const float sk = __ldg(sink + h) * kLog2e;
     const float2 *ml_row = part_ml + (size_t)r * n_split * kHeads + h;
@@ -762,13 +845,48 @@ attention_combine_kernel(const __nv_bfloat16 *__restrict__ part_o, const float2 
     }
     den += (sk == -INFINITY) ? 0.f : exp2f(sk - M);
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)r * kHeads + h) * kDim) + lane * 2;
 #pragma unroll
-    for (int e = 0; e < 2; ++e)
-        ptx::stg_v4_policy(dst + e, make_uint4(bf16x2_bits(acc[8 * e + 0] * inv, acc[8 * e + 1] * inv),
-                            bf16x2_bits(acc[8 * e + 2] * inv, acc[8 * e + 3] * inv),
-                            bf16x2_bits(acc[8 * e + 4] * inv, acc[8 * e + 5] * inv),
-                            bf16x2_bits(acc[8 * e + 6] * inv, acc[8 * e + 7] * inv)), policy);
+    for (int i = 0; i < 16; ++i) acc[i] *= inv;
+    // epilogue: lanes 28..31 hold the rope dims 448..511, 8 pairs each
+    if (epi.inv_rope) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int pair = ((lane - kNope / 16) & 3) * 8 + e;
+            const float c = __shfl_sync(0xffffffffu, cs.x, pair);
+            const float sn = __shfl_sync(0xffffffffu, cs.y, pair);
+            if (lane >= kNope / 16) {
+                const float x = acc[2 * e], y = acc[2 * e + 1];
+                acc[2 * e] = fmaf(x, c, y * sn);
+                acc[2 * e + 1] = fmaf(-x, sn, y * c);
+            }
+        }
+    }
+    if (epi.out_fp4) {
+        // E2M1 with one multiplier per 128 dims = 8 lanes
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(acc[i]));
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float sc = amax > 0.f ? amax / 6.f : 1.f;
+        uint32_t w[2];
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2)
+            w[q2] = e2m1x4(acc[8 * q2] / sc, acc[8 * q2 + 1] / sc, acc[8 * q2 + 2] / sc, acc[8 * q2 + 3] / sc) |
+                    (e2m1x4(acc[8 * q2 + 4] / sc, acc[8 * q2 + 5] / sc, acc[8 * q2 + 6] / sc, acc[8 * q2 + 7] / sc)
+                     << 16);
+        reinterpret_cast<uint2 *>(epi.out_fp4 + ((size_t)r * kHeads + h) * kFp4RowBytes)[lane] = make_uint2(w[0], w[1]);
+        if ((lane & 7) == 0) epi.out_fp4_scale[((size_t)r * kHeads + h) * 4 + (lane >> 3)] = sc;
+    } else {
+        uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)r * kHeads + h) * kDim) + lane * 2;
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+            ptx::stg_v4_policy(dst + e, make_uint4(bf16x2_bits(acc[8 * e + 0], acc[8 * e + 1]),
+                                                   bf16x2_bits(acc[8 * e + 2], acc[8 * e + 3]),
+                                                   bf16x2_bits(acc[8 * e + 4], acc[8 * e + 5]),
+                                                   bf16x2_bits(acc[8 * e + 6], acc[8 * e + 7])),
+                               policy);
+    }
     if (lane == 0) lse[(size_t)r * kHeads + h] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
 }
 
@@ -802,7 +920,8 @@ size_t attention_workspace_bytes(int B, int T, int max_selected, int W) {
 cudaError_t launch_attention(const void *q, const float *sink, float scale, const csa_cache_desc &comp,
                              const void *ring, int R, int W, const int32_t *topk_idx, const int32_t *topk_cnt,
                              const int32_t *n_comp, int m_hca, const int32_t *q_pos, int B, int T, int k, bool hca,
-                             void *out, float *lse, void *ws, size_t ws_bytes, int *err, cudaStream_t stream) {
+                             void *out, float *lse, const csa_attention_epilogue *epi, void *ws, size_t ws_bytes,
+                             int *err, cudaStream_t stream) {
     const int rows = B * T;
     const int n_split = choose_splits(rows, k + W);
     AttParams P;
@@ -828,6 +947,11 @@ cudaError_t launch_attention(const void *q, const float *sink, float scale, cons
     P.part_ml = nullptr;
     P.err = err;
     P.wait_ns = wait_limit_ns();
+    P.epi.out_fp4 = epi ? epi->out_fp4 : nullptr;
+    P.epi.out_fp4_scale = epi ? epi->out_fp4_scale : nullptr;
+    P.epi.inv_rope = (epi && epi->inverse_rope) ? 1 : 0;
+    for (int i = 0; i < kRopePairs; ++i)  // pair i turns by theta^(-2i/64) rad per position
+        P.epi.rope_freq[i] = P.epi.inv_rope ? std::pow((double)epi->rope_theta, -2.0 * i / (2.0 * kRopePairs)) : 0.0;
     if (n_split > 1) {
         const size_t need = split_bytes(rows, n_split);
         if (!ws || ws_bytes < need) return cudaErrorInvalidValue;
@@ -859,7 +983,7 @@ cudaError_t launch_attention(const void *q, const float *sink, float scale, cons
     cfg.dynamicSmemBytes = 0;
     count_launch();
     e = cudaLaunchKernelEx(&cfg, attention_combine_kernel, (const __nv_bfloat16 *)P.part_o,
-                           (const float2 *)P.part_ml, sink, n_split, P.out, lse);
+                           (const float2 *)P.part_ml, sink, n_split, P.out, lse, q_pos, P.epi);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -919,7 +1043,7 @@ extern "C" CSA_API csa_status_t csa_sink_attention_decode_noalloc(
     void *scratch = nullptr;
     if (need && static_scratch_address(&scratch) != cudaSuccess) return CSA_ERR_CUDA;
     const cudaError_t e = launch_attention(q, sink, softmax_scale, comp, swa_ring, R, W, topk_idx, topk_cnt, nullptr,
-                                           1, q_pos, B, T, k, false, out, lse, scratch,
+                                           1, q_pos, B, T, k, false, out, lse, nullptr, scratch,
                                            need ? kStaticScratchBytes : 0, status, stream);
     return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
 }

@@ -119,6 +119,35 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
+// Four floats -> four E2M1 codes in 16 bits (value i in bits 4i..4i+3): the
+// hardware conversion, round to nearest with ties to even, saturating at +-6.
+// (The instruction puts its first source in the high nibble of the byte.)
+__device__ __forceinline__ uint32_t e2m1x4(float v0, float v1, float v2, float v3) {
+    uint16_t r;
+    asm("{\n\t.reg .b8 b0, b1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "mov.b16 %0, {b0, b1};\n\t}"
+        : "=h"(r)
+        : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+    return r;
+}
+
+// cos and sin of the angle t * freq (freq in radians per position): the
+// angle is formed and reduced to [-pi, pi] in double precision (t * freq
+// reaches 10^6 rad at a 1M-token context, where a float angle would be off
+// by up to 0.03 rad), then the special-function unit's sine and cosine run on
+// the reduced angle (absolute error about 4e-7 on [-pi, pi]; no local-memory
+// slow path for large arguments).
+__device__ __forceinline__ float2 rope_cos_sin(int t, double freq) {
+    const double a = (double)t * freq;
+    const double turns = rint(a * 0.15915494309189535);  // a / (2 pi)
+    const double r = fma(-turns, 6.283185307179586, a);
+    float sn, cs;
+    __sincosf(static_cast<float>(r), &sn, &cs);
+    return make_float2(cs, sn);
+}
+
 // Order-preserving map of fp32 to uint32 (larger float -> larger key).
 __device__ __forceinline__ uint32_t order_key(float f) {
     uint32_t u = __float_as_uint(f);

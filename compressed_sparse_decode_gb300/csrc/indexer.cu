@@ -24,6 +24,9 @@
 //            by the key's scale and writes the row of logits (coalesced).
 // Keys are read once from HBM for all T tokens of a sequence; tiles past the
 // largest visible range of their sequence are never loaded (written -inf).
+// More than 4 tokens per sequence (prefill-style steps) run as token groups:
+// the kernel's "sequences" are then (sequence, group of T tokens) pairs that
+// share the sequence's keys, which each group reads again.
 // Every wait is bounded; a timeout records CSA_ERR_TIMEOUT and the CTA exits
 // after its copies and MMAs have drained.
 #include <cuda.h>
@@ -72,16 +75,18 @@ struct IdxSmem {
     int abort_flag;
 };
 
+// b: the token group (its tokens are rows b*T .. b*T+T-1 of the flattened
+// [B*T_seq] query rows); bs: its sequence (b / groups), which owns the keys.
 struct TileInfo {
-    int b;
+    int b, bs;
     int c0;
     bool skip;
 };
 
-__device__ __forceinline__ int seq_visible_max(const int32_t *q_pos, const int32_t *n_comp, int b, int T, int m,
-                                               int Ncap) {
+__device__ __forceinline__ int seq_visible_max(const int32_t *q_pos, const int32_t *n_comp, int b, int bs, int T,
+                                               int m, int Ncap) {
     int nv = 0;
-    for (int t = 0; t < T; ++t) nv = max(nv, visible_entries(__ldg(q_pos + b * T + t), m, __ldg(n_comp + b), Ncap));
+    for (int t = 0; t < T; ++t) nv = max(nv, visible_entries(__ldg(q_pos + b * T + t), m, __ldg(n_comp + bs), Ncap));
     return nv;
 }
 
@@ -90,8 +95,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                   const float *__restrict__ q_scale, const float *__restrict__ w_idx,
                   const float *__restrict__ k_scale, const int32_t *__restrict__ q_pos,
-                  const int32_t *__restrict__ n_comp, int B, int Ncap, int m, float *__restrict__ logits, int *err,
-                  uint64_t wait_ns) {
+                  const int32_t *__restrict__ n_comp, int B, int groups, int Ncap, int m,
+                  float *__restrict__ logits, int *err, uint64_t wait_ns) {
     using C = IdxCfg<T>;
     constexpr int N = C::N;
     constexpr int kHalves = C::kHalves, kTileKeys = C::kTileKeys, kStages = C::kStages, kTileBytes = C::kTileBytes;
@@ -136,22 +141,25 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     ptx::griddep_wait();
 
     // Walks this CTA's tiles in order, identically in every role, without a
-    // division per tile: sequence b, tile t within it, visible keys nv of b.
+    // division per tile: token group b (of sequence bs), tile t within it,
+    // visible keys nv of the group.
     struct Walk {
-        int b, t, nv;
+        int b, bs, t, nv;
     };
     auto walk_start = [&]() {
-        Walk w{0, 0, 0};
+        Walk w{0, 0, 0, 0};
         if (t_begin < t_end) {
             w.b = (int)(t_begin / n_tiles);
+            w.bs = w.b / groups;
             w.t = (int)(t_begin - (long)w.b * n_tiles);
-            w.nv = seq_visible_max(q_pos, n_comp, w.b, T, m, Ncap);
+            w.nv = seq_visible_max(q_pos, n_comp, w.b, w.bs, T, m, Ncap);
         }
         return w;
     };
     auto walk_info = [&](const Walk &w) {
         TileInfo ti;
         ti.b = w.b;
+        ti.bs = w.bs;
         ti.c0 = w.t * kTileKeys;
         ti.skip = ti.c0 >= w.nv;
         return ti;
@@ -159,7 +167,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     auto walk_next = [&](Walk &w) {
         if (++w.t == n_tiles) {
             w.t = 0;
-            if (++w.b < B) w.nv = seq_visible_max(q_pos, n_comp, w.b, T, m, Ncap);
+            if (++w.b < B) {
+                w.bs = w.b / groups;
+                w.nv = seq_visible_max(q_pos, n_comp, w.b, w.bs, T, m, Ncap);
+            }
         }
     };
     auto fail = [&]() {
@@ -208,7 +219,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 ptx::mbar_arrive_expect_tx(&s.full[st], kTileBytes);
 #pragma unroll
                 for (int r = 0; r < kTileKeys; r += C::kBoxRows)
-                    ptx::tma_load_2d_hint(s.keys[st] + r * kIdxDim, &kmap, &s.full[st], 0, ti.b * Ncap + ti.c0 + r,
+                    ptx::tma_load_2d_hint(s.keys[st] + r * kIdxDim, &kmap, &s.full[st], 0, ti.bs * Ncap + ti.c0 + r,
                                           policy);
             }
             __syncwarp();
@@ -295,7 +306,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 #pragma unroll
                 for (int hm = 0; hm < kHalves; ++hm) {
                     const int c = ti.c0 + 128 * hm + row;
-                    sk_next[hm] = c < Ncap ? __ldg(k_scale + (size_t)ti.b * Ncap + c) : 0.f;
+                    sk_next[hm] = c < Ncap ? __ldg(k_scale + (size_t)ti.bs * Ncap + c) : 0.f;
                 }
                 return;
             }
@@ -318,7 +329,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 active_b = ti.b;
                 if (!wait(&s.q_full[u & 1], (u >> 1) & 1)) { fail(); ok = false; break; }
                 for (int t = 0; t < T; ++t)
-                    nvis[t] = visible_entries(__ldg(q_pos + ti.b * T + t), m, __ldg(n_comp + ti.b), Ncap);
+                    nvis[t] = visible_entries(__ldg(q_pos + ti.b * T + t), m, __ldg(n_comp + ti.bs), Ncap);
                 ++u;
             }
             const uint32_t my_a = a++;
@@ -443,19 +454,21 @@ bool cached_rows128_map(CUtensorMap *map, const void *base, uint64_t rows, uint3
     return true;
 }
 
+// T tokens per group, `groups` groups per sequence (T * groups tokens each).
 template <int T>
 cudaError_t launch_t(const uint8_t *q_idx, const float *q_scale, const float *w_idx, const uint8_t *k_idx,
-                     const float *k_scale, const int32_t *q_pos, const int32_t *n_comp, int B, int Ncap, int m,
-                     float *logits, int *err, cudaStream_t stream) {
+                     const float *k_scale, const int32_t *q_pos, const int32_t *n_comp, int B, int groups, int Ncap,
+                     int m, float *logits, int *err, cudaStream_t stream) {
     using C = IdxCfg<T>;
     CUtensorMap kmap, qmap;
     if (!cached_rows128_map(&kmap, k_idx, (uint64_t)B * Ncap, C::kBoxRows) ||
-        !cached_rows128_map(&qmap, q_idx, (uint64_t)B * T * kIdxHeads, T * kIdxHeads))
+        !cached_rows128_map(&qmap, q_idx, (uint64_t)B * groups * T * kIdxHeads, T * kIdxHeads))
         return cudaErrorInvalidValue;
+    const int Bg = B * groups;  // token groups: the kernel's sequences
     const size_t smem = sizeof(IdxSmem<T>) + 1024;
     cudaError_t e = set_max_dynamic_smem_once(reinterpret_cast<const void *>(indexer_tc_kernel<T>), (int)smem);
     if (e != cudaSuccess) return e;
-    const long tiles = (long)B * ((Ncap + C::kTileKeys - 1) / C::kTileKeys);
+    const long tiles = (long)Bg * ((Ncap + C::kTileKeys - 1) / C::kTileKeys);
     const int grid = (int)std::min<long>(tiles, cached_sm_count());
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -468,8 +481,8 @@ cudaError_t launch_t(const uint8_t *q_idx, const float *q_scale, const float *w_
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
     count_launch();
-    e = cudaLaunchKernelEx(&cfg, indexer_tc_kernel<T>, kmap, qmap, q_scale, w_idx, k_scale, q_pos, n_comp, B, Ncap, m,
-                           logits, err, wait_limit_ns());
+    e = cudaLaunchKernelEx(&cfg, indexer_tc_kernel<T>, kmap, qmap, q_scale, w_idx, k_scale, q_pos, n_comp, Bg, groups,
+                           Ncap, m, logits, err, wait_limit_ns());
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -479,11 +492,14 @@ cudaError_t launch_t(const uint8_t *q_idx, const float *q_scale, const float *w_
 cudaError_t launch_indexer(const uint8_t *q_idx, const float *q_scale, const float *w_idx, const uint8_t *k_idx,
                            const float *k_scale, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap,
                            int m, float *logits, int *err, cudaStream_t stream) {
-    switch (T) {
-    case 1: return launch_t<1>(q_idx, q_scale, w_idx, k_idx, k_scale, q_pos, n_comp, B, Ncap, m, logits, err, stream);
-    case 2: return launch_t<2>(q_idx, q_scale, w_idx, k_idx, k_scale, q_pos, n_comp, B, Ncap, m, logits, err, stream);
-    case 3: return launch_t<3>(q_idx, q_scale, w_idx, k_idx, k_scale, q_pos, n_comp, B, Ncap, m, logits, err, stream);
-    case 4: return launch_t<4>(q_idx, q_scale, w_idx, k_idx, k_scale, q_pos, n_comp, B, Ncap, m, logits, err, stream);
+    // tokens per group: the largest of 4, 3, 2, 1 that divides T
+    const int tg = (T % 4 == 0) ? 4 : (T % 3 == 0) ? 3 : (T % 2 == 0) ? 2 : 1;
+    const int groups = T / tg;
+    switch (tg) {
+    case 1: return launch_t<1>(q_idx, q_scale, w_idx, k_idx, k_scale, q_pos, n_comp, B, groups, Ncap, m, logits, err, stream);
+    case 2: return launch_t<2>(q_idx, q_scale, w_idx, k_idx, k_scale, q_pos, n_comp, B, groups, Ncap, m, logits, err, stream);
+    case 3: return launch_t<3>(q_idx, q_scale, w_idx, k_idx, k_scale, q_pos, n_comp, B, groups, Ncap, m, logits, err, stream);
+    case 4: return launch_t<4>(q_idx, q_scale, w_idx, k_idx, k_scale, q_pos, n_comp, B, groups, Ncap, m, logits, err, stream);
     }
     return cudaErrorInvalidValue;
 }

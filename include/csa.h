@@ -74,7 +74,7 @@ extern "C" {
 #define CSA_RECORD_BYTES 592
 #define CSA_INDEXER_HEADS 64
 #define CSA_INDEXER_DIM 128
-#define CSA_MAX_TOKENS_PER_SEQ 4 /* T: query tokens per sequence and step */
+#define CSA_MAX_TOKENS_PER_SEQ 128 /* T: query tokens per sequence and step */
 #define CSA_MAX_TOPK 2048
 #define CSA_MAX_SWA_WINDOW 512 /* W */
 
@@ -131,7 +131,11 @@ CSA_API size_t csa_workspace_bytes(csa_op_t op, int B, int T, int Ncap, int k);
  *   w_idx       [B,T,64] fp32               k_idx [B,Ncap,128] e4m3 codes
  *   k_idx_scale [B,Ncap] fp32 (> 0)          q_pos [B,T] int32, n_comp [B] int32
  *   logits      [B,T,Ncap] fp32 (written in full)
- * Requires 1 <= T <= 4, Ncap >= 1, m >= 1. Accumulation is fp32. */
+ * Requires 1 <= T <= CSA_MAX_TOKENS_PER_SEQ, Ncap >= 1, m >= 1. Accumulation
+ * is fp32. Up to 4 tokens of a sequence share one read of its keys; larger T
+ * (a prefill-style step, "ROADMAP -- Stage E" section E8) runs as groups of
+ * up to 4 tokens (the largest of 4, 3, 2, 1 dividing T), each reading the
+ * keys again. */
 CSA_API csa_status_t csa_indexer_logits(const uint8_t *q_idx, const float *q_idx_scale, const float *w_idx,
                                 const uint8_t *k_idx, const float *k_idx_scale,
                                 const int32_t *q_pos, const int32_t *n_comp,
@@ -199,6 +203,53 @@ CSA_API csa_status_t hca_sink_attention_decode(const void *q, const float *sink,
                                        int B, int T, int m_hca, void *out, float *lse,
                                        void *workspace, size_t workspace_bytes, int32_t *status,
                                        cudaStream_t stream);
+
+/* Output epilogue of the attention ("DSV4 Audit" section A4: the attention
+ * output is turned back by RoPE(-t) at the query position t, which makes the
+ * absolute positions carried by the summed latents relative; "ROADMAP --
+ * Stage E" section E6: the output may leave the attention as FP4 E2M1 with a
+ * per-128-element block amax, packed inside the same launch). Used by the
+ * _ex entry points; NULL there means plain BF16 output.
+ *   inverse_rope   nonzero: the rope dims of every head's output, pair i =
+ *                  dims (448 + 2i, 449 + 2i), i < 32, are turned back by
+ *                  a = t * rope_theta^(-2i/64) radians, t = q_pos[b,t]:
+ *                    x' = x cos a + y sin a,   y' = -x sin a + y cos a
+ *                  (the pages fix no RoPE convention; this pairing and
+ *                  frequency schedule are this library's reading)
+ *   rope_theta     RoPE base, > 1 (e.g. 10000); read only with inverse_rope
+ *   out_fp4        NULL: BF16 output in `out`. Otherwise device
+ *                  [B,T,128,256] bytes, 16-byte aligned: the E2M1 codes of
+ *                  the 512 output dims (after the rotation), dim 2i in the
+ *                  low nibble of byte i; `out` is not written and may be NULL
+ *   out_fp4_scale  with out_fp4: device [B,T,128,4] fp32, 16-byte aligned:
+ *                  s = amax / 6 of output dims [128 j, 128 j + 128) (1 when
+ *                  they are all zero); code = the E2M1 value nearest to
+ *                  value / s (ties to even, saturating at 6), so that
+ *                  value ~ e2m1(code) * s */
+typedef struct {
+    int32_t inverse_rope;
+    float rope_theta;
+    uint8_t *out_fp4;
+    float *out_fp4_scale;
+} csa_attention_epilogue;
+
+/* csa_sink_attention_decode / hca_sink_attention_decode with an output
+ * epilogue (see csa_attention_epilogue); identical to them when `epilogue`
+ * is NULL or asks for neither step. Same workspace sizes. A bad epilogue
+ * (theta <= 1 with inverse_rope, out_fp4 without out_fp4_scale, misaligned
+ * pointers) returns CSA_ERR_INVALID_ARG before any launch. */
+CSA_API csa_status_t csa_sink_attention_decode_ex(const void *q, const float *sink, float softmax_scale,
+                                                  csa_cache_desc comp, const void *swa_ring, int R, int W,
+                                                  const int32_t *topk_idx, const int32_t *topk_cnt,
+                                                  const int32_t *q_pos, int B, int T, int k, void *out, float *lse,
+                                                  const csa_attention_epilogue *epilogue, void *workspace,
+                                                  size_t workspace_bytes, int32_t *status, cudaStream_t stream);
+CSA_API csa_status_t hca_sink_attention_decode_ex(const void *q, const float *sink, float softmax_scale,
+                                                  csa_cache_desc comp, const int32_t *n_comp, const void *swa_ring,
+                                                  int R, int W, const int32_t *q_pos, int B, int T, int m_hca,
+                                                  void *out, float *lse, const csa_attention_epilogue *epilogue,
+                                                  void *workspace, size_t workspace_bytes, int32_t *status,
+                                                  cudaStream_t stream);
 
 /* Allocation-free variant of csa_sink_attention_decode (the pages have no
  * counterpart; it exists for callers of this library that cannot allocate

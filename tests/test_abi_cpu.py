@@ -59,7 +59,7 @@ def test_host_validation_rejects_before_launch(lib):
     # null pointers
     assert lib.csa_indexer_logits(None, None, None, None, None, None, None, 1, 1, 8, 4, None, None, None) == csd.ERR_INVALID_ARG
     # T beyond the supported maximum
-    assert lib.csa_indexer_logits(fake, fake, fake, fake, fake, fake, fake, 1, 5, 8, 4, fake, None, None) == csd.ERR_INVALID_ARG
+    assert lib.csa_indexer_logits(fake, fake, fake, fake, fake, fake, fake, 1, 129, 8, 4, fake, None, None) == csd.ERR_INVALID_ARG
     # misaligned logits pointer
     assert lib.csa_indexer_logits(fake, fake, fake, fake, fake, fake, fake, 1, 1, 8, 4, P(0x1004), None, None) == csd.ERR_INVALID_ARG
     # k larger than the capacity / the maximum
@@ -94,7 +94,7 @@ def test_pipeline_staging_sizes(lib):
     assert csd.csa_pipeline_staging_bytes(B, T, 3) == 3 * one
     assert csd.csa_pipeline_staging_bytes(B, T, 1) == 0          # depth below 2
     assert csd.csa_pipeline_staging_bytes(B, T, 5) == 0          # depth above the maximum
-    assert csd.csa_pipeline_staging_bytes(B, 5, 2) == 0          # T above the maximum
+    assert csd.csa_pipeline_staging_bytes(B, 129, 2) == 0        # T above the maximum
     assert csd.csa_pipeline_staging_bytes(0, 1, 2) == 0
 
 
@@ -174,7 +174,7 @@ def test_noalloc_rejects_like_the_workspace_call(lib):
     over.base, over.n_records, over.seq_stride, over.seq_capacity = 0x1000, 100, 5, 10
     cases = [
         dict(q=None), dict(comp=bad_cache), dict(comp=over, B=2), dict(W=600, R=600), dict(R=64),
-        dict(scale=0.0), dict(k=4096), dict(T=5), dict(out=C.c_void_p(0x1008)),
+        dict(scale=0.0), dict(k=4096), dict(T=129), dict(out=C.c_void_p(0x1008)),
     ]
     for c in cases:
         a = dict(q=fake, comp=good, R=128, W=128, B=1, T=1, k=4, out=fake, scale=0.1)
@@ -184,6 +184,41 @@ def test_noalloc_rejects_like_the_workspace_call(lib):
         ws_status = lib.csa_sink_attention_decode(*common, None, 0, None, None)
         na_status = lib.csa_sink_attention_decode_noalloc(*common, None, None)
         assert ws_status == na_status != csd.OK, c
+
+
+def test_epilogue_entry_points_validate_before_launch(lib):
+    """The _ex calls check the same arguments as the plain calls (a NULL
+    epilogue gives the same status) and reject a bad epilogue up front."""
+    fake = C.c_void_p(0x1000)
+    good = csd.csa_cache_desc()
+    good.base, good.n_records, good.seq_stride, good.seq_capacity = 0x1000, 10, 10, 10
+    for c in [dict(q=None), dict(R=64), dict(scale=0.0), dict(k=4096), dict(T=129), dict(out=C.c_void_p(0x1008))]:
+        a = dict(q=fake, R=128, W=128, T=1, k=4, out=fake, scale=0.1)
+        a.update(c)
+        common = (a["q"], fake, C.c_float(a["scale"]), good, fake, a["R"], a["W"], fake, fake, fake, 1, a["T"], a["k"],
+                  a["out"], fake)
+        plain = lib.csa_sink_attention_decode(*common, None, 0, None, None)
+        ex = lib.csa_sink_attention_decode_ex(*common, None, None, 0, None, None)
+        assert plain == ex != csd.OK, c
+    common = (fake, fake, C.c_float(0.1), good, fake, 128, 128, fake, fake, fake, 1, 1, 4)
+    hca_common = (fake, fake, C.c_float(0.1), good, fake, fake, 128, 128, fake, 1, 1, 128)
+    E = csd.csa_attention_epilogue
+    bad = [E(1, 1.0, None, None),                 # theta must exceed 1
+           E(1, float("nan"), None, None),
+           E(0, 0.0, 0x2000, None),               # E2M1 output without its multipliers
+           E(0, 0.0, 0x2008, 0x3000),             # misaligned E2M1 output
+           E(0, 0.0, 0x2000, 0x3004)]             # misaligned multipliers
+    for e in bad:
+        assert lib.csa_sink_attention_decode_ex(*common, fake, fake, C.byref(e), None, 0, None, None) == \
+            csd.ERR_INVALID_ARG
+        assert lib.hca_sink_attention_decode_ex(*hca_common, fake, fake, C.byref(e), None, 0, None, None) == \
+            csd.ERR_INVALID_ARG
+    # without E2M1 output `out` is required; with it, `out` may be NULL (then a later check fails: no ring)
+    assert lib.csa_sink_attention_decode_ex(*common, None, fake, C.byref(E(1, 1e4, None, None)), None, 0, None,
+                                            None) == csd.ERR_INVALID_ARG
+    nor = (fake, fake, C.c_float(0.1), good, None, 128, 128, fake, fake, fake, 1, 1, 4)
+    assert lib.csa_sink_attention_decode_ex(*nor, None, fake, C.byref(E(0, 0.0, 0x2000, 0x3000)), None, 0, None,
+                                            None) == csd.ERR_INVALID_ARG
 
 
 def test_product_path_does_not_import_the_oracle():
