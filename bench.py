@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--report-configs", action="store_true",
                     help="print one JSON line of per-kernel times for every workload instead of the benchmark line")
+    ap.add_argument("--epilogue", action="store_true",
+                    help="time the attention with its output epilogues (inverse RoPE, E2M1 output)")
     ap.add_argument("--prefill", type=int, default=0, metavar="T",
                     help="time T tokens of one 128K sequence as one step against T single-token steps")
     ap.add_argument("--graph-replay", type=int, default=0, metavar="LAYERS",
@@ -777,8 +779,9 @@ def prefill(args):
     section E8: prefill spread over many CTAs): T consecutive tokens of one
     128K-context sequence (top-2048) as one csa_decode_step over B*T rows,
     against the same tokens issued as T single-token steps (one query row per
-    launch). Device time with CUDA events on the calling stream, median of 20
-    after 3 warm-ups."""
+    launch). Each variant is replayed from a CUDA graph (no host call overhead
+    in the device time); CUDA events on the replay stream, median of 20 after 3
+    warm-ups."""
     import torch
 
     import compressed_sparse_decode_gb300 as csd
@@ -808,21 +811,35 @@ def prefill(args):
             csd.csa_decode_step(qi, qs, wi, x.k_idx, x.k_idx_scale, q, x.sink, SCALE, comp, x.ring, wl.W, qp, x.n_comp,
                                 wl.m, wl.k, out=o, lse=l, ws=ws1)
 
-    def timed(fn, n=20):
-        for _ in range(3):
+    # each variant captured once into a CUDA graph, so that the host's call
+    # overhead (a Python call per step) does not enter the device time
+    stream = torch.cuda.Stream(device=dev)
+
+    def graphed(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
             fn()
+        return g
+
+    def timed(g, n=20):
         ts = []
-        for _ in range(n):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize(dev)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize(dev)
-            ts.append(a.elapsed_time(b) * 1e3)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            for _ in range(n):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                b.synchronize()
+                ts.append(a.elapsed_time(b) * 1e3)
         return float(statistics.median(ts))
 
-    t_b, t_l = timed(batched), timed(token_loop)
+    t_b, t_l = timed(graphed(batched)), timed(graphed(token_loop))
     if csd.csa_read_device_error():
         raise RuntimeError("device error word set")
     # the batched step's rows agree with the single-token steps' rows
@@ -835,9 +852,76 @@ def prefill(args):
                                   "clock": "CUDA events, median of 20 after 3 warm-ups"}}), flush=True)
 
 
+def epilogue_timing(args):
+    """The attention's output epilogue ("DSV4 Audit" section A4, "ROADMAP --
+    Stage E" section E6) on the 128K and HCA workloads: the attention call
+    with BF16 output, with the inverse RoPE, with E2M1 output, and with both.
+    Device time with CUDA events around 10 back-to-back calls, median of 20
+    after 3 warm-ups, inputs resident (the same call repeated); output bytes
+    per call alongside."""
+    import torch
+
+    import compressed_sparse_decode_gb300 as csd
+    import synth
+    csd.build()
+    csd.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    res = {}
+    for name in ("csa_b32_ctx128k_k2048", "hca_b64_ctx1m"):
+        x = synth.generate(name, seed=0, device=dev)
+        wl = x.wl
+        comp = csd.cache_desc(x.comp, wl.ncap, x.seq_stride)
+        rows = wl.B * wl.T
+        if wl.kind == "csa":
+            lg = csd.csa_indexer_logits(x.q_idx, x.q_idx_scale, x.w_idx, x.k_idx, x.k_idx_scale, x.q_pos, x.n_comp,
+                                        wl.m)
+            idx, cnt = csd.csa_topk(lg, x.q_pos, x.n_comp, wl.m, wl.k)
+            ws = csd.workspace(csd.OP_ATTENTION, wl.B, wl.T, wl.ncap, wl.k, dev)
+            call = lambda **e: csd.csa_sink_attention_decode(x.q, x.sink, SCALE, comp, x.ring, wl.W, idx, cnt,
+                                                             x.q_pos, ws=ws, **e)
+        else:
+            ws = csd.workspace(csd.OP_HCA_ATTENTION, wl.B, wl.T, wl.ncap, 0, dev)
+            call = lambda **e: csd.hca_sink_attention_decode(x.q, x.sink, SCALE, comp, x.n_comp, x.ring, wl.W,
+                                                             x.q_pos, wl.m, ws=ws, **e)
+        out = torch.empty_like(x.q)
+        f4 = torch.empty((wl.B, wl.T, 128, 256), dtype=torch.uint8, device=dev)
+        f4s = torch.empty((wl.B, wl.T, 128, 4), dtype=torch.float32, device=dev)
+        variants = {"bf16": dict(out=out), "bf16+inverse_rope": dict(out=out, inverse_rope=True),
+                    "e2m1": dict(fp4_out=True, out_fp4=f4, out_fp4_scale=f4s),
+                    "e2m1+inverse_rope": dict(fp4_out=True, out_fp4=f4, out_fp4_scale=f4s, inverse_rope=True)}
+        row = {}
+        for v, kw in variants.items():
+            for _ in range(3):
+                call(**kw)
+            ts = []
+            for _ in range(20):
+                # 10 calls back to back per event pair: the device stays busy
+                # while the host issues the next call
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize(dev)
+                a.record()
+                for _ in range(10):
+                    call(**kw)
+                b.record()
+                torch.cuda.synchronize(dev)
+                ts.append(a.elapsed_time(b) * 1e3 / 10)
+            out_bytes = rows * 128 * (512 * 2 if v.startswith("bf16") else 256 + 16)
+            row[v] = {"us": round(statistics.median(ts), 2), "output_bytes": out_bytes}
+        if csd.csa_read_device_error():
+            raise RuntimeError("device error word set")
+        res[name] = row
+    print(json.dumps({"epilogue": res, "clock": "CUDA events around 10 back-to-back calls, median of 20"}),
+          flush=True)
+
+
 def main():
     args = parse()
     rank, world, local_rank = dist_env()
+    if args.epilogue:
+        if rank == 0:
+            epilogue_timing(args)
+        return
     if args.prefill:
         if rank == 0:
             prefill(args)

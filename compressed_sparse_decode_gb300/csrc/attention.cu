@@ -734,6 +734,7 @@ attention_tc_kernel(const AttParams P) {
                         for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
                     }
                     const float sc = amax > 0.f ? amax / 6.f : 1.f;
+                    const float inv = 1.f / sc;  // value / sc as value * (1 / sc): equal up to one ulp
 #pragma unroll 1
                     for (int pp = 0; pp < 4; ++pp) {
                         float v[32];
@@ -741,9 +742,10 @@ attention_tc_kernel(const AttParams P) {
                         uint32_t w[4];
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4)
-                            w[q4] = e2m1x4(v[8 * q4] / sc, v[8 * q4 + 1] / sc, v[8 * q4 + 2] / sc, v[8 * q4 + 3] / sc) |
-                                    (e2m1x4(v[8 * q4 + 4] / sc, v[8 * q4 + 5] / sc, v[8 * q4 + 6] / sc,
-                                            v[8 * q4 + 7] / sc) << 16);
+                            w[q4] = e2m1x4(v[8 * q4] * inv, v[8 * q4 + 1] * inv, v[8 * q4 + 2] * inv,
+                                           v[8 * q4 + 3] * inv) |
+                                    (e2m1x4(v[8 * q4 + 4] * inv, v[8 * q4 + 5] * inv, v[8 * q4 + 6] * inv,
+                                            v[8 * q4 + 7] * inv) << 16);
                         const int c = 4 * bl + pp;
                         *reinterpret_cast<uint4 *>(frow + ((c ^ (h & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
                     }
@@ -869,12 +871,13 @@ attention_combine_kernel(const __nv_bfloat16 *__restrict__ part_o, const float2 
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         const float sc = amax > 0.f ? amax / 6.f : 1.f;
+        const float isc = 1.f / sc;  // value / sc as value * (1 / sc): equal up to one ulp
         uint32_t w[2];
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2)
-            w[q2] = e2m1x4(acc[8 * q2] / sc, acc[8 * q2 + 1] / sc, acc[8 * q2 + 2] / sc, acc[8 * q2 + 3] / sc) |
-                    (e2m1x4(acc[8 * q2 + 4] / sc, acc[8 * q2 + 5] / sc, acc[8 * q2 + 6] / sc, acc[8 * q2 + 7] / sc)
-                     << 16);
+            w[q2] = e2m1x4(acc[8 * q2] * isc, acc[8 * q2 + 1] * isc, acc[8 * q2 + 2] * isc, acc[8 * q2 + 3] * isc) |
+                    (e2m1x4(acc[8 * q2 + 4] * isc, acc[8 * q2 + 5] * isc, acc[8 * q2 + 6] * isc,
+                            acc[8 * q2 + 7] * isc) << 16);
         reinterpret_cast<uint2 *>(epi.out_fp4 + ((size_t)r * kHeads + h) * kFp4RowBytes)[lane] = make_uint2(w[0], w[1]);
         if ((lane & 7) == 0) epi.out_fp4_scale[((size_t)r * kHeads + h) * 4 + (lane >> 3)] = sc;
     } else {
