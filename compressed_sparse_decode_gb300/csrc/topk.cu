@@ -2,22 +2,29 @@
 // ("DSV4 Audit", section B2; "ROADMAP -- Stage E", section E7: top-k with
 // warp-level reductions and no global lock).
 //
-// One row (query token) per cluster of 8 CTAs of 512 threads (1024 for rows
-// above 64K entries); CTA rank c owns the slice [c * slice, (c + 1) * slice)
-// of the row, and thread t of a CTA owns the contiguous run of
-// E = slice / threads entries starting at t * E (kept in shared
-// memory transposed, keys[j][t], so every access is conflict-free). The CTA
-// loads its slice once as order-preserving 32-bit keys; a radix select then
-// finds the k-th largest key K* in three digit passes (bits 31..21, 20..10,
-// 9..0): per pass every CTA builds a histogram of its matching keys in its own
-// shared memory, and after a cluster barrier each thread sums 4 bins over the
-// 8 CTAs through distributed shared memory; a block-wide scan over the bins
-// (largest digit first) picks the digit, identically in every CTA. Finally
-// each CTA keeps its keys > K* and, in index order, the lowest-index keys ==
-// K* still needed: per-thread counts are scanned, the per-CTA totals are
-// exchanged through rank 0, and every thread writes its run at its global
+// Two kernels. The 8-bit radix select below (topk_radix8_kernel) serves every
+// row whose keys fit in the shared memory of one cluster (up to 360448
+// entries); the 11-bit cluster kernel that follows serves longer rows, its
+// keys read from global memory in every pass when they do not fit.
+//
+// Cluster kernel: one row (query token) per cluster of 8 CTAs of 512 threads
+// (1024 for rows above 64K entries); CTA rank c owns the slice
+// [c * slice, (c + 1) * slice) of the row, and thread t of a CTA owns the
+// contiguous run of E = slice / threads entries starting at t * E (kept in
+// shared memory transposed, keys[j][t], so every access is conflict-free). The
+// CTA loads its slice once as order-preserving 32-bit keys; a radix select
+// then finds the k-th largest key K* in three digit passes (bits 31..21,
+// 20..10, 9..0): per pass every CTA builds a histogram of its matching keys in
+// its own shared memory, and after a cluster barrier each thread sums 4 bins
+// over the 8 CTAs through distributed shared memory; a block-wide scan over
+// the bins (largest digit first) picks the digit, identically in every CTA.
+// Finally each CTA keeps its keys > K* and, in index order, the lowest-index
+// keys == K* still needed: per-thread counts are scanned, the per-CTA totals
+// are exchanged through rank 0, and every thread writes its run at its global
 // offset, so the output is in ascending index order. No lock and no global
 // atomic is used.
+#include <mutex>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -280,11 +287,13 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
     ptx::cluster_sync();  // no CTA leaves while another may still read rank 0's counts
 }
 
-// ------------------------------------------------------------------ 8-bit radix select, short rows
+// ------------------------------------------------------------------ 8-bit radix select
 //
-// One row per cluster of C = 1, 2, 4 or 8 CTAs (the smallest that holds the
-// row at <= 32 keys per thread), so a row of 32768 entries is one CTA with no
-// cluster barrier at all. The radix select takes four 8-bit digit passes
+// One row per cluster of C CTAs (256 threads each up to 65536 entries, 1024
+// above): C is the smallest power of two up to 8 that holds the row at <= 8
+// keys a thread, lowered (C = 7, 6, ...) while the rows' clusters would not
+// all be resident at once and the keys still fit (<= 44 a thread). The radix
+// select takes four 8-bit digit passes
 // (bits 31..24, 23..16, 15..8, 7..0 of the order-preserving key). The top
 // digit of float keys is the sign and the high exponent bits, so nearly all
 // keys share two or three values of it and a histogram of it serialises on a
@@ -295,13 +304,12 @@ topk_cluster_kernel(const float *__restrict__ logits, const int32_t *__restrict_
 // histogram, which keeps collisions within a warp. Per pass the warp histograms are summed
 // into the CTA's, the C CTA histograms are summed through distributed shared
 // memory after one cluster barrier (double-buffered by pass parity, so one
-// barrier per pass suffices), and one warp picks the digit, identically in
-// every CTA. The compaction is the one above: keys > K*, then the
+// barrier per pass suffices; each thread issues its C remote loads together,
+// one round trip), and one warp picks the digit, identically in every CTA. The compaction is the one above: keys > K*, then the
 // lowest-index keys == K* while the budget lasts, in ascending index order.
-constexpr int kR8MaxRun = 32;
+constexpr int kR8MaxRun = 44;  // keys per thread held in shared memory (212 KB at 1024 threads)
 constexpr int kR8MaxCtas = 8;
 constexpr int kR8TargetRun = 8;  // keys per thread the cluster width aims at (up to 8 CTAs)
-constexpr int kR8SmallRow = 8192;  // rows this long or shorter use this kernel
 
 template <int kThreads>
 struct Radix8Shared {
@@ -416,9 +424,14 @@ topk_radix8_kernel(const float *__restrict__ logits, const int32_t *__restrict__
         sync_all();
         uint32_t top = s.cta_top[0][0];
         if (clustered) {
+            // every CTA's maximum, loaded together (one round trip), then reduced
             const uint32_t a = ptx::smem_u32(&s.cta_top[0][0]);
+            uint32_t v[kR8MaxCtas];
+#pragma unroll
+            for (int c = 0; c < kR8MaxCtas; ++c) v[c] = c < (int)nctas ? ld_cluster_u32(ptx::mapa(a, c)) : 0u;
             top = 0u;
-            for (uint32_t c = 0; c < nctas; ++c) top = max(top, ld_cluster_u32(ptx::mapa(a, c)));
+#pragma unroll
+            for (int c = 0; c < kR8MaxCtas; ++c) top = max(top, v[c]);
         }
         const uint32_t tdig = top >> 24;
         // four 8-bit counters in one register (a thread holds <= 32 keys)
@@ -446,15 +459,26 @@ topk_radix8_kernel(const float *__restrict__ logits, const int32_t *__restrict__
             s.cta_top[1][tid] = (uint32_t)c;
         }
         sync_all();
+        // window counts over the cluster: lane 8 d + c loads CTA c's count of
+        // digit tdig - d (all 32 loads in flight together), then a reduction
+        // over each group of 8 lanes
+        if (warp == 0) {
+            const int d = lane >> 3, c = lane & 7;
+            uint32_t v = 0u;
+            if (clustered) {
+                if (c < (int)nctas) v = ld_cluster_u32(ptx::mapa(ptx::smem_u32(&s.cta_top[1][d]), (uint32_t)c));
+            } else if (c == 0) {
+                v = s.cta_top[1][d];
+            }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (c == 0) s.wwin[0][d] = (int)v;
+        }
+        __syncthreads();
         if (tid == 0) {
             int cum = 0, found = 0;
             for (int d = 0; d < 4 && !found; ++d) {
-                int cd = (int)s.cta_top[1][d];
-                if (clustered) {
-                    const uint32_t a = ptx::smem_u32(&s.cta_top[1][d]);
-                    cd = 0;
-                    for (uint32_t c = 0; c < nctas; ++c) cd += (int)ld_cluster_u32(ptx::mapa(a, c));
-                }
+                const int cd = s.wwin[0][d];
                 if ((int)tdig - d >= 0 && cum + cd >= remaining) {
                     s.digit = tdig - (uint32_t)d;
                     s.remaining = remaining - cum;
@@ -500,9 +524,14 @@ topk_radix8_kernel(const float *__restrict__ logits, const int32_t *__restrict__
         if (tid < 256) {
             uint32_t total = s.cta_hist[pass & 1][tid];
             if (clustered) {
+                // every CTA's count of this bin, loaded together (one round trip)
                 const uint32_t a = ptx::smem_u32(&s.cta_hist[pass & 1][tid]);
+                uint32_t v[kR8MaxCtas];
+#pragma unroll
+                for (int c = 0; c < kR8MaxCtas; ++c) v[c] = c < (int)nctas ? ld_cluster_u32(ptx::mapa(a, c)) : 0u;
                 total = 0;
-                for (uint32_t c = 0; c < nctas; ++c) total += ld_cluster_u32(ptx::mapa(a, c));
+#pragma unroll
+                for (int c = 0; c < kR8MaxCtas; ++c) total += v[c];
             }
             s.hist[tid] = total;
         }
@@ -632,32 +661,81 @@ cudaError_t launch_t(const float *logits, const int32_t *q_pos, const int32_t *n
 
 }  // namespace
 
+// Clusters of `kernel` (launched as `cfg`, one cluster's worth of CTAs) that
+// the device holds at once, looked up once per device, kernel and size.
+int max_active_clusters(const void *kernel, cudaLaunchConfig_t cfg, int ctas) {
+    struct Entry {
+        const void *kernel;
+        int dev, ctas;
+        size_t smem;
+        int n;
+    };
+    static Entry cache[32];
+    static int used = 0;
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> g(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].kernel == kernel && cache[i].dev == dev && cache[i].ctas == ctas &&
+            cache[i].smem == cfg.dynamicSmemBytes)
+            return cache[i].n;
+    int n = 0;
+    cfg.gridDim = dim3(ctas);
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();  // a failed query reads as "does not fit"
+        n = 0;
+    }
+    if (used < 32) cache[used++] = {kernel, dev, ctas, cfg.dynamicSmemBytes, n};
+    return n;
+}
+
 template <int kThreads>
 cudaError_t launch_r8(const float *logits, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap, int m,
                       int k, int32_t *idx_out, int32_t *cnt_out, cudaStream_t stream) {
+    const void *kernel = reinterpret_cast<const void *>(topk_radix8_kernel<kThreads>);
+    auto run_for = [&](int c) {
+        const int r = ((Ncap + c - 1) / c + kThreads - 1) / kThreads;
+        return (r + 3) & ~3;  // whole groups of 4 (16-byte copies)
+    };
     int ctas = 1;
     while ((Ncap + ctas - 1) / ctas > kThreads * kR8TargetRun && ctas < kR8MaxCtas) ctas *= 2;
-    int run = ((Ncap + ctas - 1) / ctas + kThreads - 1) / kThreads;
-    run = (run + 3) & ~3;  // whole groups of 4 (16-byte copies)
-    const size_t smem = sizeof(Radix8Shared<kThreads>) + (size_t)run * kThreads * sizeof(uint32_t);
+    if (run_for(ctas) > kR8MaxRun) return cudaErrorInvalidValue;  // rows longer than the kernel holds
     const size_t smem_max = sizeof(Radix8Shared<kThreads>) + (size_t)kR8MaxRun * kThreads * sizeof(uint32_t);
-    cudaError_t e =
-        set_max_dynamic_smem_once(reinterpret_cast<const void *>(topk_radix8_kernel<kThreads>), (int)smem_max);
+    cudaError_t e = set_max_dynamic_smem_once(kernel, (int)smem_max);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(B * T * ctas);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the indexer ends
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = ctas;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
+    auto configure = [&](int c) {
+        attr[1].val.clusterDim.x = c;
+        cfg.dynamicSmemBytes = sizeof(Radix8Shared<kThreads>) + (size_t)run_for(c) * kThreads * sizeof(uint32_t);
+    };
+    // All rows' clusters should be resident at once: a second wave doubles
+    // the time (measured for 16 rows of 262144 entries in 8-CTA clusters of
+    // one SM each: 15 clusters resident, 28 -> 55 us). Fewer, fuller CTAs per
+    // row fit more clusters beside each other.
+    configure(ctas);
+    if (ctas > 1 && max_active_clusters(kernel, cfg, ctas) < B * T) {
+        for (int c = ctas - 1; c >= 2 && run_for(c) <= kR8MaxRun; --c) {
+            configure(c);
+            if (max_active_clusters(kernel, cfg, c) >= B * T) {
+                ctas = c;
+                break;
+            }
+        }
+        configure(ctas);
+    }
+    const int run = run_for(ctas);
+    cfg.gridDim = dim3(B * T * ctas);
     count_launch();
     e = cudaLaunchKernelEx(&cfg, topk_radix8_kernel<kThreads>, logits, q_pos, n_comp, T, Ncap, m, k, run, idx_out,
                            cnt_out);
@@ -667,13 +745,19 @@ cudaError_t launch_r8(const float *logits, const int32_t *q_pos, const int32_t *
 
 cudaError_t launch_topk(const float *logits, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap,
                         int m, int k, int32_t *idx_out, int32_t *cnt_out, void *, size_t, cudaStream_t stream) {
-    // Rows up to 8192 entries: the 8-bit radix select (measured: 8.1 against
-    // 14.2 us for 256-entry rows, 13.3 against 14.3 us for 8192). Longer rows:
-    // the 11-bit cluster kernel, which measured as fast or faster there (20.0
-    // against 20.4-28.6 us for 32768-entry rows with 1 to 8 CTAs a row, 58 against
-    // 55-58 us for 262144).
-    if (Ncap <= kR8SmallRow)
-        return launch_r8<256>(logits, q_pos, n_comp, B, T, Ncap, m, k, idx_out, cnt_out, stream);
+    // Rows whose keys fit in the shared memory of a cluster (up to 8 x 1024
+    // threads x 44 keys): the 8-bit radix select, 256 threads a CTA up to
+    // 65536 entries, 1024 above. Measured against the 11-bit cluster kernel
+    // (events around 20 calls on rotating inputs): 8.1 against 14.2 us for
+    // 256-entry rows, 13.6 against 14.3 us for 8192, 18.8 against 19.9 us for
+    // 32768, 37.4 against 58.7 us for 262144 (where 8-CTA clusters of one SM
+    // each left one of the 16 rows for a second wave). Longer rows: the
+    // cluster kernel, whose keys may stay in global memory.
+    if (Ncap <= kR8MaxCtas * 1024 * kR8MaxRun) {
+        if (Ncap <= kR8MaxCtas * 256 * 32)
+            return launch_r8<256>(logits, q_pos, n_comp, B, T, Ncap, m, k, idx_out, cnt_out, stream);
+        return launch_r8<1024>(logits, q_pos, n_comp, B, T, Ncap, m, k, idx_out, cnt_out, stream);
+    }
     const int per_cta = (Ncap + kCtas - 1) / kCtas;
     if ((per_cta + 511) / 512 > kRunSplit)
         return launch_t<1024>(logits, q_pos, n_comp, B, T, Ncap, m, k, idx_out, cnt_out, stream);
