@@ -312,21 +312,32 @@ constexpr int kR8MaxCtas = 8;
 constexpr int kR8TargetRun = 8;  // keys per thread the cluster width aims at (up to 8 CTAs)
 
 template <int kThreads>
-struct Radix8Shared {
+struct alignas(16) Radix8Shared {  // the keys follow it as 16-byte groups
     static constexpr int kWarps = kThreads / 32;
     uint32_t whist[kWarps][256];       // per-warp histograms of the current pass
-    uint32_t cta_hist[2][256];         // this CTA's histogram, by pass parity (read by the peers)
+    // Every CTA's partial results, each written into every CTA of the cluster
+    // by its owner before a cluster barrier, so that after the barrier every
+    // CTA reads them from its own shared memory (no remote loads on the
+    // critical path, and no remote access at all after the last barrier).
+    uint16_t peer_hist[2][kR8MaxCtas][256];  // per-CTA histogram of a pass (<= 45056 keys a CTA), by pass parity
+    uint32_t peer_top[kR8MaxCtas];           // per-CTA largest key
+    uint32_t peer_win[kR8MaxCtas][4];        // per-CTA counts of the top-digit window
+    int peer_counts[kR8MaxCtas][2];          // per-CTA (keys > K*, keys == K*)
     uint32_t hist[256];                // the row's histogram of the current pass
-    alignas(16) int counts[kR8MaxCtas][2];  // rank 0's copy: (keys > K*, keys == K*) per CTA
-    alignas(16) int peer_counts[kR8MaxCtas][2];
     int wsum[kWarps];
     uint32_t wmax[kWarps];             // per-warp largest key
-    uint32_t cta_top[2][5];            // this CTA's (largest key, window counts) (read by the peers)
     int wwin[kWarps][4];               // per-warp counts of the keys in the top-digit window
     uint32_t digit;
     int remaining;
     int fallback;                      // pass 0 needs the histogram
 };
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
 
 __device__ __forceinline__ uint32_t cluster_nctarank() {
     uint32_t r;
@@ -334,11 +345,6 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
     return r;
 }
 
-__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
-}
 
 template <int kThreads>
 __global__ void __launch_bounds__(kThreads)
@@ -346,6 +352,7 @@ topk_radix8_kernel(const float *__restrict__ logits, const int32_t *__restrict__
                    const int32_t *__restrict__ n_comp, int T, int Ncap, int m, int k, int run,
                    int32_t *__restrict__ idx_out, int32_t *__restrict__ cnt_out) {
     using S = Radix8Shared<kThreads>;
+    static_assert(sizeof(S) % 16 == 0, "the keys after the shared struct must be 16-byte aligned");
     extern __shared__ __align__(16) uint8_t smem_raw[];
     S &s = *reinterpret_cast<S *>(smem_raw);
     // keys4[g][t]: the g-th group of 4 consecutive entries of thread t's run
@@ -406,6 +413,8 @@ topk_radix8_kernel(const float *__restrict__ logits, const int32_t *__restrict__
 
     uint32_t prefix = 0, mask = 0;
     int remaining = k;
+    // `field` of this CTA's shared memory, in CTA c of the cluster
+    auto in_cta = [&](const void *field, int c) { return ptx::mapa(ptx::smem_u32(field), (uint32_t)c); };
     // ---- pass 0 through the window below the largest key's top digit
     {
         uint32_t mx = 0u;
@@ -416,25 +425,16 @@ topk_radix8_kernel(const float *__restrict__ logits, const int32_t *__restrict__
         mx = __reduce_max_sync(0xffffffffu, mx);
         if (lane == 0) s.wmax[warp] = mx;
         __syncthreads();
-        if (tid == 0) {
+        if (tid < (int)nctas) {  // thread c gives CTA c this CTA's largest key
             uint32_t m2 = 0u;
             for (int w = 0; w < S::kWarps; ++w) m2 = max(m2, s.wmax[w]);
-            s.cta_top[0][0] = m2;
+            st_cluster_u32(in_cta(&s.peer_top[crank], tid), m2);
         }
         sync_all();
-        uint32_t top = s.cta_top[0][0];
-        if (clustered) {
-            // every CTA's maximum, loaded together (one round trip), then reduced
-            const uint32_t a = ptx::smem_u32(&s.cta_top[0][0]);
-            uint32_t v[kR8MaxCtas];
-#pragma unroll
-            for (int c = 0; c < kR8MaxCtas; ++c) v[c] = c < (int)nctas ? ld_cluster_u32(ptx::mapa(a, c)) : 0u;
-            top = 0u;
-#pragma unroll
-            for (int c = 0; c < kR8MaxCtas; ++c) top = max(top, v[c]);
-        }
+        uint32_t top = 0u;
+        for (int c = 0; c < (int)nctas; ++c) top = max(top, s.peer_top[c]);
         const uint32_t tdig = top >> 24;
-        // four 8-bit counters in one register (a thread holds <= 32 keys)
+        // four 8-bit counters in one register (a thread holds <= 44 keys)
         uint32_t packed = 0u;
         auto win = [&](uint32_t key) {
             const uint32_t d = tdig - (key >> 24);
@@ -453,32 +453,18 @@ topk_radix8_kernel(const float *__restrict__ logits, const int32_t *__restrict__
             if (lane == 0) s.wwin[warp][d] = c;
         }
         __syncthreads();
-        if (tid < 4) {
+        if (tid < 4 * (int)nctas) {  // thread 4 c + d gives CTA c this CTA's count of digit tdig - d
+            const int d = tid & 3;
             int c = 0;
-            for (int w = 0; w < S::kWarps; ++w) c += s.wwin[w][tid];
-            s.cta_top[1][tid] = (uint32_t)c;
+            for (int w = 0; w < S::kWarps; ++w) c += s.wwin[w][d];
+            st_cluster_u32(in_cta(&s.peer_win[crank][d], tid >> 2), (uint32_t)c);
         }
         sync_all();
-        // window counts over the cluster: lane 8 d + c loads CTA c's count of
-        // digit tdig - d (all 32 loads in flight together), then a reduction
-        // over each group of 8 lanes
-        if (warp == 0) {
-            const int d = lane >> 3, c = lane & 7;
-            uint32_t v = 0u;
-            if (clustered) {
-                if (c < (int)nctas) v = ld_cluster_u32(ptx::mapa(ptx::smem_u32(&s.cta_top[1][d]), (uint32_t)c));
-            } else if (c == 0) {
-                v = s.cta_top[1][d];
-            }
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (c == 0) s.wwin[0][d] = (int)v;
-        }
-        __syncthreads();
         if (tid == 0) {
             int cum = 0, found = 0;
             for (int d = 0; d < 4 && !found; ++d) {
-                const int cd = s.wwin[0][d];
+                int cd = 0;
+                for (int c = 0; c < (int)nctas; ++c) cd += (int)s.peer_win[c][d];
                 if ((int)tdig - d >= 0 && cum + cd >= remaining) {
                     s.digit = tdig - (uint32_t)d;
                     s.remaining = remaining - cum;
@@ -515,24 +501,19 @@ topk_radix8_kernel(const float *__restrict__ logits, const int32_t *__restrict__
         }
         __syncthreads();  // every warp histogram of this pass is complete
         if (tid < 256) {
+            // this CTA's count of bin `tid`, given to every CTA (buffer by
+            // pass parity: a CTA reads buffer p & 1 before it arrives at the
+            // barrier of pass p + 1, and nobody writes it again before then)
             uint32_t sum = 0;
 #pragma unroll 8
             for (int w = 0; w < S::kWarps; ++w) sum += s.whist[w][tid];
-            s.cta_hist[pass & 1][tid] = sum;
+            for (int c = 0; c < (int)nctas; ++c)
+                st_cluster_u16(in_cta(&s.peer_hist[pass & 1][crank][tid], c), (uint16_t)sum);
         }
-        sync_all();  // every CTA histogram of this pass is complete
+        sync_all();  // every CTA's histogram of this pass has arrived
         if (tid < 256) {
-            uint32_t total = s.cta_hist[pass & 1][tid];
-            if (clustered) {
-                // every CTA's count of this bin, loaded together (one round trip)
-                const uint32_t a = ptx::smem_u32(&s.cta_hist[pass & 1][tid]);
-                uint32_t v[kR8MaxCtas];
-#pragma unroll
-                for (int c = 0; c < kR8MaxCtas; ++c) v[c] = c < (int)nctas ? ld_cluster_u32(ptx::mapa(a, c)) : 0u;
-                total = 0;
-#pragma unroll
-                for (int c = 0; c < kR8MaxCtas; ++c) total += v[c];
-            }
+            uint32_t total = 0;
+            for (int c = 0; c < (int)nctas; ++c) total += s.peer_hist[pass & 1][c][tid];
             s.hist[tid] = total;
         }
         __syncthreads();
@@ -584,14 +565,13 @@ topk_radix8_kernel(const float *__restrict__ logits, const int32_t *__restrict__
     const int gt_excl = (int)(excl >> 16), eq_excl = (int)(excl & 0xFFFFu);
     int base = 0, eq_before = 0;
     if (clustered) {
-        const uint32_t counts0 = ptx::mapa(ptx::smem_u32(&s.counts[0][0]), 0);
-        if (tid == 0) {
-            st_cluster_s32(counts0 + crank * 8, (int)(tot_packed >> 16));
-            st_cluster_s32(counts0 + crank * 8 + 4, (int)(tot_packed & 0xFFFFu));
+        if (tid < (int)nctas) {  // thread c gives CTA c this CTA's totals
+            st_cluster_u32(in_cta(&s.peer_counts[crank][0], tid), tot_packed >> 16);
+            st_cluster_u32(in_cta(&s.peer_counts[crank][1], tid), tot_packed & 0xFFFFu);
         }
+        // the last barrier: no CTA touches another's shared memory after it,
+        // so each may leave as soon as it is done
         ptx::cluster_sync();
-        if (tid < kR8MaxCtas * 2 / 4) reinterpret_cast<uint4 *>(&s.peer_counts[0][0])[tid] = ld_cluster_v4(counts0 + tid * 16);
-        __syncthreads();
         for (int c = 0; c < (int)crank; ++c) {
             const int ce = s.peer_counts[c][1];
             base += s.peer_counts[c][0] + min(max(remaining - eq_before, 0), ce);
@@ -619,7 +599,6 @@ topk_radix8_kernel(const float *__restrict__ logits, const int32_t *__restrict__
         emit(v.w, 4 * g + 3);
     }
     if (crank == 0 && tid == 0) cnt_out[r] = k;
-    if (clustered) ptx::cluster_sync();  // no CTA leaves while another may still read its shared memory
 }
 
 }  // namespace
