@@ -353,20 +353,21 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 ptx::tmem_ld32(col + 32, r1);
                 ptx::tmem_ld_wait();
                 const float4 *w4 = reinterpret_cast<const float4 *>(ws + t * kIdxHeads);
-                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+                // two heads per packed FMA (each lane an IEEE fma: the same
+                // sums as four scalar chains s0..s3)
+                float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
+                auto relu2 = [](uint32_t a, uint32_t b) {
+                    return make_float2(fmaxf(__uint_as_float(a), 0.f), fmaxf(__uint_as_float(b), 0.f));
+                };
 #pragma unroll
                 for (int h4 = 0; h4 < 8; ++h4) {
                     const float4 wa = w4[h4], wb = w4[8 + h4];
-                    s0 = fmaf(wa.x, fmaxf(__uint_as_float(r0[4 * h4 + 0]), 0.f), s0);
-                    s1 = fmaf(wa.y, fmaxf(__uint_as_float(r0[4 * h4 + 1]), 0.f), s1);
-                    s0 = fmaf(wa.z, fmaxf(__uint_as_float(r0[4 * h4 + 2]), 0.f), s0);
-                    s1 = fmaf(wa.w, fmaxf(__uint_as_float(r0[4 * h4 + 3]), 0.f), s1);
-                    s2 = fmaf(wb.x, fmaxf(__uint_as_float(r1[4 * h4 + 0]), 0.f), s2);
-                    s3 = fmaf(wb.y, fmaxf(__uint_as_float(r1[4 * h4 + 1]), 0.f), s3);
-                    s2 = fmaf(wb.z, fmaxf(__uint_as_float(r1[4 * h4 + 2]), 0.f), s2);
-                    s3 = fmaf(wb.w, fmaxf(__uint_as_float(r1[4 * h4 + 3]), 0.f), s3);
+                    s01 = __ffma2_rn(make_float2(wa.x, wa.y), relu2(r0[4 * h4 + 0], r0[4 * h4 + 1]), s01);
+                    s01 = __ffma2_rn(make_float2(wa.z, wa.w), relu2(r0[4 * h4 + 2], r0[4 * h4 + 3]), s01);
+                    s23 = __ffma2_rn(make_float2(wb.x, wb.y), relu2(r1[4 * h4 + 0], r1[4 * h4 + 1]), s23);
+                    s23 = __ffma2_rn(make_float2(wb.z, wb.w), relu2(r1[4 * h4 + 2], r1[4 * h4 + 3]), s23);
                 }
-                acc[hm][t] = (s0 + s1) + (s2 + s3);
+                acc[hm][t] = (s01.x + s01.y) + (s23.x + s23.y);
             }
             ptx::tc_fence_before();
             __syncwarp();
