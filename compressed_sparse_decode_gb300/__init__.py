@@ -32,7 +32,7 @@ EXPORTED = ["csa_workspace_bytes", "csa_indexer_logits", "csa_topk", "csa_gather
             "csa_status_string", "csa_version", "csa_kernel_launches",
             "csa_sink_attention_decode_noalloc", "csa_pipeline_staging_bytes", "csa_pipeline_create",
             "csa_decode_step_host", "csa_pipeline_wait", "csa_pipeline_sync", "csa_pipeline_destroy",
-            "csa_sink_attention_decode_ex", "hca_sink_attention_decode_ex"]
+            "csa_sink_attention_decode_ex", "hca_sink_attention_decode_ex", "csa_decode_step_ex"]
 PIPELINE_MAX_DEPTH = 4
 
 
@@ -100,6 +100,9 @@ def load(path: str | None = None):
         lib.hca_sink_attention_decode_ex.argtypes = ([P, P, f32, csa_cache_desc, P, P, i32, i32, P, i32, i32, i32,
                                                       P, P, EP, P, sz, P, P])
         lib.hca_sink_attention_decode_ex.restype = st
+        lib.csa_decode_step_ex.argtypes = ([P] * 7 + [f32, csa_cache_desc, P, i32, i32, P, P] + [i32] * 5
+                                           + [P, P, P, P, EP, P, sz, P, P])
+        lib.csa_decode_step_ex.restype = st
         lib.csa_pipeline_staging_bytes.argtypes = [i32, i32, i32]
         lib.csa_pipeline_staging_bytes.restype = sz
         lib.csa_pipeline_create.argtypes = [C.POINTER(C.c_void_p), i32, i32, i32, P, sz, P]
@@ -378,32 +381,37 @@ def hca_sink_attention_decode(q, sink, softmax_scale: float, comp: csa_cache_des
 
 def csa_decode_step(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q, sink, softmax_scale: float,
                     comp: csa_cache_desc, swa_ring, W: int, q_pos, n_comp, m: int, k: int, out=None, lse=None,
-                    topk_idx=None, topk_cnt=None, ws=None, stream=None, status=None):
+                    topk_idx=None, topk_cnt=None, ws=None, stream=None, status=None, inverse_rope: bool = False,
+                    rope_theta: float = 10000.0, fp4_out: bool = False, out_fp4=None, out_fp4_scale=None):
+    """Returns (out, lse); with fp4_out, ((out_fp4, out_fp4_scale), lse)."""
     B, T = q_pos.shape
     Ncap = k_idx.shape[1]
     R = swa_ring.shape[1]
     dev = q.device
-    if out is None:
+    epi, out_fp4, out_fp4_scale = _epilogue(B, T, dev, inverse_rope, rope_theta, fp4_out, out_fp4, out_fp4_scale)
+    if out is None and not fp4_out:
         out = torch.empty((B, T, HEADS, DIM), dtype=torch.bfloat16, device=dev)
     if lse is None:
         lse = torch.empty((B, T, HEADS), dtype=torch.float32, device=dev)
     if ws is None:
         ws = workspace(OP_DECODE_STEP, B, T, Ncap, k, dev)
     u8 = (torch.uint8, torch.float8_e4m3fn)
-    _check(load().csa_decode_step(
-        _ptr(q_idx, "q_idx", u8, (B, T, IDX_HEADS, IDX_DIM)),
-        _ptr(q_idx_scale, "q_idx_scale", torch.float32, (B, T, IDX_HEADS)),
-        _ptr(w_idx, "w_idx", torch.float32, (B, T, IDX_HEADS)), _ptr(k_idx, "k_idx", u8, (B, Ncap, IDX_DIM)),
-        _ptr(k_idx_scale, "k_idx_scale", torch.float32, (B, Ncap)),
-        _ptr(q, "q", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(sink, "sink", torch.float32, (HEADS,)),
-        float(softmax_scale), comp, _ptr(swa_ring, "swa_ring", torch.uint8, (B, R, RECORD_BYTES)), R, int(W),
-        _ptr(q_pos, "q_pos", torch.int32, (B, T)), _ptr(n_comp, "n_comp", torch.int32, (B,)),
-        B, T, Ncap, int(m), int(k),
-        _ptr(out, "out", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(lse, "lse", torch.float32, (B, T, HEADS)),
-        _ptr(topk_idx, "topk_idx", torch.int32, (B, T, k)), _ptr(topk_cnt, "topk_cnt", torch.int32, (B, T)),
-        _ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _status(status, dev), _stream(stream)),
-        "csa_decode_step")
-    return out, lse
+    args = [_ptr(q_idx, "q_idx", u8, (B, T, IDX_HEADS, IDX_DIM)),
+            _ptr(q_idx_scale, "q_idx_scale", torch.float32, (B, T, IDX_HEADS)),
+            _ptr(w_idx, "w_idx", torch.float32, (B, T, IDX_HEADS)), _ptr(k_idx, "k_idx", u8, (B, Ncap, IDX_DIM)),
+            _ptr(k_idx_scale, "k_idx_scale", torch.float32, (B, Ncap)),
+            _ptr(q, "q", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(sink, "sink", torch.float32, (HEADS,)),
+            float(softmax_scale), comp, _ptr(swa_ring, "swa_ring", torch.uint8, (B, R, RECORD_BYTES)), R, int(W),
+            _ptr(q_pos, "q_pos", torch.int32, (B, T)), _ptr(n_comp, "n_comp", torch.int32, (B,)),
+            B, T, Ncap, int(m), int(k),
+            _ptr(out, "out", torch.bfloat16, (B, T, HEADS, DIM)), _ptr(lse, "lse", torch.float32, (B, T, HEADS)),
+            _ptr(topk_idx, "topk_idx", torch.int32, (B, T, k)), _ptr(topk_cnt, "topk_cnt", torch.int32, (B, T))]
+    tail = [_ptr(ws, "workspace", torch.uint8), 0 if ws is None else ws.numel(), _status(status, dev), _stream(stream)]
+    if epi is None:
+        _check(load().csa_decode_step(*args, *tail), "csa_decode_step")
+    else:
+        _check(load().csa_decode_step_ex(*args, C.byref(epi), *tail), "csa_decode_step_ex")
+    return ((out_fp4, out_fp4_scale) if fp4_out else out), lse
 
 
 def _hptr(t: torch.Tensor, name: str, dtype, shape):

@@ -300,17 +300,19 @@ csa_status_t hca_sink_attention_decode(const void *q, const float *sink, float s
                                         lse, nullptr, workspace, workspace_bytes, status, stream);
 }
 
-csa_status_t csa_decode_step(const uint8_t *q_idx, const float *q_idx_scale, const float *w_idx,
-                             const uint8_t *k_idx, const float *k_idx_scale, const void *q, const float *sink,
-                             float softmax_scale, csa_cache_desc comp, const void *swa_ring, int R, int W,
-                             const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap, int m, int k,
-                             void *out, float *lse, int32_t *topk_idx, int32_t *topk_cnt, void *workspace,
-                             size_t workspace_bytes, int32_t *status, cudaStream_t stream) {
+csa_status_t csa_decode_step_ex(const uint8_t *q_idx, const float *q_idx_scale, const float *w_idx,
+                                const uint8_t *k_idx, const float *k_idx_scale, const void *q, const float *sink,
+                                float softmax_scale, csa_cache_desc comp, const void *swa_ring, int R, int W,
+                                const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap, int m, int k,
+                                void *out, float *lse, int32_t *topk_idx, int32_t *topk_cnt,
+                                const csa_attention_epilogue *epilogue, void *workspace, size_t workspace_bytes,
+                                int32_t *status, cudaStream_t stream) {
     // every argument of the three calls is checked before the first launch
-    const csa_status_t a =
-        csa::decode_step_arg_status(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q, sink, softmax_scale, comp,
-                                    swa_ring, R, W, q_pos, n_comp, B, T, Ncap, m, k, out, lse, topk_idx,
-                                    workspace, workspace_bytes, status);
+    csa_status_t a = epilogue_status(epilogue, out);
+    if (a != CSA_OK) return a;
+    a = csa::decode_step_arg_status(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q, sink, softmax_scale, comp,
+                                    swa_ring, R, W, q_pos, n_comp, B, T, Ncap, m, k, checked_out(epilogue, out), lse,
+                                    topk_idx, workspace, workspace_bytes, status);
     if (a != CSA_OK) return a;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     float *logits = reinterpret_cast<float *>(ws);
@@ -328,8 +330,19 @@ csa_status_t csa_decode_step(const uint8_t *q_idx, const float *q_idx_scale, con
     if (s != CSA_OK) return s;
     s = csa_topk(logits, q_pos, n_comp, B, T, Ncap, m, k, idx, cnt, tk_ws, tk_bytes, status, stream);
     if (s != CSA_OK) return s;
-    return csa_sink_attention_decode(q, sink, softmax_scale, comp, swa_ring, R, W, idx, cnt, q_pos, B, T, k, out, lse,
-                                     at_bytes ? ws : nullptr, at_bytes, status, stream);
+    return csa_sink_attention_decode_ex(q, sink, softmax_scale, comp, swa_ring, R, W, idx, cnt, q_pos, B, T, k, out,
+                                        lse, epilogue, at_bytes ? ws : nullptr, at_bytes, status, stream);
+}
+
+csa_status_t csa_decode_step(const uint8_t *q_idx, const float *q_idx_scale, const float *w_idx,
+                             const uint8_t *k_idx, const float *k_idx_scale, const void *q, const float *sink,
+                             float softmax_scale, csa_cache_desc comp, const void *swa_ring, int R, int W,
+                             const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap, int m, int k,
+                             void *out, float *lse, int32_t *topk_idx, int32_t *topk_cnt, void *workspace,
+                             size_t workspace_bytes, int32_t *status, cudaStream_t stream) {
+    return csa_decode_step_ex(q_idx, q_idx_scale, w_idx, k_idx, k_idx_scale, q, sink, softmax_scale, comp, swa_ring,
+                              R, W, q_pos, n_comp, B, T, Ncap, m, k, out, lse, topk_idx, topk_cnt, nullptr, workspace,
+                              workspace_bytes, status, stream);
 }
 
 csa_status_t csa_check_device_status(int32_t *status, int32_t *host_status, cudaStream_t stream) {

@@ -293,6 +293,21 @@ CSA_API csa_status_t csa_decode_step(const uint8_t *q_idx, const float *q_idx_sc
                              void *out, float *lse, int32_t *topk_idx, int32_t *topk_cnt,
                              void *workspace, size_t workspace_bytes, int32_t *status, cudaStream_t stream);
 
+/* csa_decode_step with the attention's output epilogue
+ * (csa_attention_epilogue; NULL = csa_decode_step): the step's last kernel
+ * writes the inverse-RoPE'd and/or E2M1 output ("ROADMAP -- Stage E",
+ * section E6: the quantised output leaves the attention in the same launch).
+ * With E2M1 output `out` may be NULL. Checks as csa_decode_step plus those of
+ * csa_sink_attention_decode_ex, all before the first launch. */
+CSA_API csa_status_t csa_decode_step_ex(const uint8_t *q_idx, const float *q_idx_scale, const float *w_idx,
+                                        const uint8_t *k_idx, const float *k_idx_scale, const void *q,
+                                        const float *sink, float softmax_scale, csa_cache_desc comp,
+                                        const void *swa_ring, int R, int W, const int32_t *q_pos,
+                                        const int32_t *n_comp, int B, int T, int Ncap, int m, int k, void *out,
+                                        float *lse, int32_t *topk_idx, int32_t *topk_cnt,
+                                        const csa_attention_epilogue *epilogue, void *workspace,
+                                        size_t workspace_bytes, int32_t *status, cudaStream_t stream);
+
 /* Host-I/O decode pipeline (the pages have no counterpart; it serves callers
  * whose query-side inputs arrive in, and whose results go back to, host
  * memory). csa_decode_step_host runs csa_decode_step on per-step copies of

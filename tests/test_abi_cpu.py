@@ -221,6 +221,25 @@ def test_epilogue_entry_points_validate_before_launch(lib):
                                             None) == csd.ERR_INVALID_ARG
 
 
+def test_decode_step_ex_checks_its_epilogue_before_launching(lib):
+    fake = C.c_void_p(0x1000)
+    good = csd.csa_cache_desc()
+    good.base, good.n_records, good.seq_stride, good.seq_capacity = 0x1000, 10, 10, 10
+    args = (fake, fake, fake, fake, fake, fake, fake, C.c_float(0.1), good, fake, 128, 128, fake, fake, 1, 1, 10, 4, 4)
+    E = csd.csa_attention_epilogue
+    # a bad epilogue is reported before the missing workspace
+    assert lib.csa_decode_step_ex(*args, fake, fake, None, None, C.byref(E(1, 0.5, None, None)), None, 0, None,
+                                  None) == csd.ERR_INVALID_ARG
+    assert lib.csa_decode_step_ex(*args, None, fake, None, None, C.byref(E(0, 0.0, 0x2000, None)), None, 0, None,
+                                  None) == csd.ERR_INVALID_ARG
+    # NULL epilogue: the same status as csa_decode_step
+    assert lib.csa_decode_step_ex(*args, fake, fake, None, None, None, None, 0, None, None) == \
+        lib.csa_decode_step(*args, fake, fake, None, None, None, 0, None, None) == csd.ERR_WORKSPACE
+    # E2M1 output stands in for `out`
+    assert lib.csa_decode_step_ex(*args, None, fake, None, None, C.byref(E(0, 0.0, 0x2000, 0x3000)), None, 0, None,
+                                  None) == csd.ERR_WORKSPACE
+
+
 def test_product_path_does_not_import_the_oracle():
     pkg = os.path.join(ROOT, "compressed_sparse_decode_gb300")
     for dirpath, _, files in os.walk(pkg):

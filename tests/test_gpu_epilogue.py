@@ -34,7 +34,11 @@ pytestmark = pytest.mark.gpu
 THREADS = os.cpu_count() or 1
 SCALE = 1.0 / math.sqrt(512)
 THETA = 10000.0
-CASES = {"csa_b1_ctx1k_k64": [0], "csa_b8_ctx16k32k_k512": [0, 5], "hca_b64_ctx1m": [0, 37, 63]}
+CASES = {"csa_b1_ctx1k_k64": [0], "csa_b8_ctx16k32k_k512": [0, 5], "hca_b64_ctx1m": [0, 37, 63],
+         "csa_b2t4_ctx20k_k128": [0, 3, 5, 7]}
+# a small multi-token workload: 4 tokens a sequence, each with its own position (and rotation)
+CUSTOM = {"csa_b2t4_ctx20k_k128": synth.custom("csa", B=2, T=4, ncap=5000, k=128, ctx=20000,
+                                              name="csa_b2t4_ctx20k_k128")}
 # E2M1 rounding boundaries (midpoints between neighbouring magnitudes)
 BOUNDS = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
 E2M1 = np.array([oracle.e2m1_value(c) for c in range(16)])
@@ -46,7 +50,7 @@ def _setup(csd, name):
     if name not in _cache:
         _cache.clear()
         torch.cuda.empty_cache()
-        x = synth.generate(name, seed=3, device="cuda")
+        x = synth.generate(CUSTOM.get(name, name), seed=3, device="cuda")
         comp = csd.cache_desc(x.comp, x.wl.ncap, x.seq_stride)
         if x.wl.kind == "csa":
             lg = csd.csa_indexer_logits(x.q_idx, x.q_idx_scale, x.w_idx, x.k_idx, x.k_idx_scale, x.q_pos, x.n_comp,
@@ -93,28 +97,28 @@ def _unpack(packed):
     return codes
 
 
-@pytest.mark.parametrize("name", list(CASES))
-def test_inverse_rope_bf16(cuda_lib, name):
+@pytest.mark.parametrize("name,theta", [(n, THETA) for n in CASES] + [("csa_b8_ctx16k32k_k512", 1.0e6)])
+def test_inverse_rope_bf16(cuda_lib, name, theta):
     csd = cuda_lib
     rows = CASES[name]
     plain, lse0 = _attend(csd, name)
-    out, lse = _attend(csd, name, inverse_rope=True, rope_theta=THETA)
+    out, lse = _attend(csd, name, inverse_rope=True, rope_theta=theta)
     torch.cuda.synchronize()
     assert csd.csa_read_device_error() == 0
     assert torch.equal(out[..., :448], plain[..., :448]) and torch.equal(lse, lse0)
     B, T = out.shape[:2]
     # the rotation itself: the plain output turned back in fp64
     pos_all = _cache[name][0].q_pos.cpu().numpy().reshape(-1)
-    want = oracle.inverse_rope(plain.float().cpu().numpy().reshape(B * T, 128, 512), pos_all, THETA)
+    want = oracle.inverse_rope(plain.float().cpu().numpy().reshape(B * T, 128, 512), pos_all, theta)
     got = out.float().cpu().numpy().reshape(B * T, 128, 512)
     mag = np.abs(plain.float().cpu().numpy().reshape(B * T, 128, 512)[..., 448:])
     pair_mag = np.repeat(np.hypot(mag[..., 0::2], mag[..., 1::2]), 2, axis=-1)
     assert np.all(np.abs(got[..., 448:] - want[..., 448:]) <= 2 ** -7 * pair_mag + 1e-30)
     # against the oracle's output turned back by the oracle
     oo, ol, pos, tol = _oracle(name, rows)
-    ref = oracle.inverse_rope(oo, pos, THETA)
+    ref = oracle.inverse_rope(oo, pos, theta)
     stats = check_attention(got[rows], lse.cpu().numpy().reshape(-1, 128)[rows], ref, ol, f"{name} inverse rope", tol)
-    print(f"{name} inverse rope: min cos {stats[0]:.6f}  max rel {stats[1]:.3g}")
+    print(f"{name} inverse rope (theta {theta:g}): min cos {stats[0]:.6f}  max rel {stats[1]:.3g}")
 
 
 def _near_bound(v, rel):
@@ -161,3 +165,20 @@ def test_fp4_output(cuda_lib, name, rope):
           f"min cos to the exact output {cos_gpu.min():.5f} (oracle-quantised {cos_fmt.min():.5f}); "
           f"largest per-head shortfall {float((cos_fmt - cos_gpu).max()):.2e}")
     assert np.all(cos_gpu >= cos_fmt - 1e-3)
+
+
+@pytest.mark.parametrize("name", ["csa_b8_ctx16k32k_k512", "csa_b2t4_ctx20k_k128"])
+def test_decode_step_with_epilogue_equals_separate_calls(cuda_lib, name):
+    csd = cuda_lib
+    x, comp, idx, cnt = _setup(csd, name)
+    wl = x.wl
+    epi = dict(inverse_rope=True, rope_theta=THETA, fp4_out=True)
+    (p1, s1), l1 = _attend(csd, name, **epi)
+    sidx, scnt = torch.empty_like(idx), torch.empty_like(cnt)
+    (p2, s2), l2 = csd.csa_decode_step(x.q_idx, x.q_idx_scale, x.w_idx, x.k_idx, x.k_idx_scale, x.q, x.sink, SCALE,
+                                       comp, x.ring, wl.W, x.q_pos, x.n_comp, wl.m, wl.k, topk_idx=sidx,
+                                       topk_cnt=scnt, **epi)
+    torch.cuda.synchronize()
+    assert csd.csa_read_device_error() == 0
+    assert torch.equal(sidx, idx) and torch.equal(scnt, cnt)
+    assert torch.equal(p1, p2) and torch.equal(s1, s2) and torch.equal(l1, l2)
