@@ -229,6 +229,16 @@ attention_tc_kernel(const AttParams P) {
     const int rank = blockIdx.x & 1;  // output half: 0 = lo, 1 = hi
     volatile int *abort = &s.abort_flag;
 
+    // The query rows are an input, not produced by the kernels before this one:
+    // their prefetch into L2 starts at once, before the wait for the top-k
+    // (the prefetch is a hint; the loads themselves follow the wait).
+    if (threadIdx.x == 32 * 9) {  // the otherwise idle warp
+        const uint8_t *qrow = reinterpret_cast<const uint8_t *>(P.q) +
+                              (size_t)((blockIdx.x >> 1) / P.n_split) * kHeads * kDim * sizeof(__nv_bfloat16);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ptx::prefetch_l2_bulk(qrow + i * 16384, 16384u);
+        static_assert(kHeads * kDim * sizeof(__nv_bfloat16) == 8 * 16384, "one query's rows are 8 x 16 KB");
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < kPtrRing; ++i) {
             ptx::mbar_init(&s.ptr_full[i], 32);  // every producer lane has written its pointers
@@ -522,8 +532,8 @@ attention_tc_kernel(const AttParams P) {
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const int r = u.r;
         bool ok = true;
-        // Q: dims 256..511 -> shared memory (cp.async), dims 0..255 -> TMEM
-        // (BF16 pairs, lane = head), 128 dims per round trip
+        // Q: the dims from kQTmemDims up -> shared memory (cp.async), the
+        // dims below -> TMEM (BF16 pairs, lane = head)
         if (u.n_chunks > 0) {
             const uint4 *qg = reinterpret_cast<const uint4 *>(P.q + ((size_t)r * kHeads + h) * kDim);
             // every byte a decode step reads or writes once is marked
@@ -534,23 +544,34 @@ attention_tc_kernel(const AttParams P) {
             for (int c = 0; c < (kDim - kQTmemDims) / 8; ++c)
                 ptx::cp_async_16_hint(sw128(s.qs + (c >> 3) * kQAtom, h, c & 7), qg + kQTmemDims / 8 + c, q_policy);
             ptx::cp_async_commit();
-#pragma unroll 1
-            for (int pp = 0; pp < kQTmemDims / 128; ++pp) {
-                uint4 w[16];
+            // pieces of 64 dims (128 B a thread, 32 TMEM columns), two in
+            // flight: piece p + 2 is requested as soon as piece p has gone to
+            // TMEM
+            constexpr int kQPieces = kQTmemDims / 64;
+            uint4 wa[8], wb[8];
+            auto load_piece = [&](uint4 (&w)[8], int pc) {
 #pragma unroll
-                for (int v = 0; v < 16; ++v) w[v] = ptx::ldg_v4_policy(qg + pp * 16 + v, q_policy);
+                for (int v = 0; v < 8; ++v) w[v] = ptx::ldg_v4_policy(qg + pc * 8 + v, q_policy);
+            };
+            auto store_piece = [&](const uint4 (&w)[8], int pc) {
+                uint32_t regs[32];
 #pragma unroll
-                for (int hp = 0; hp < 2; ++hp) {
-                    uint32_t regs[32];
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        regs[4 * v] = w[8 * hp + v].x;
-                        regs[4 * v + 1] = w[8 * hp + v].y;
-                        regs[4 * v + 2] = w[8 * hp + v].z;
-                        regs[4 * v + 3] = w[8 * hp + v].w;
-                    }
-                    ptx::tmem_st32(lane_base + kColQ + (2 * pp + hp) * 32, regs);
+                for (int v = 0; v < 8; ++v) {
+                    regs[4 * v] = w[v].x;
+                    regs[4 * v + 1] = w[v].y;
+                    regs[4 * v + 2] = w[v].z;
+                    regs[4 * v + 3] = w[v].w;
                 }
+                ptx::tmem_st32(lane_base + kColQ + pc * 32, regs);
+            };
+            load_piece(wa, 0);
+            load_piece(wb, 1);
+#pragma unroll 1
+            for (int pc = 0; pc < kQPieces; pc += 2) {
+                store_piece(wa, pc);
+                if (pc + 2 < kQPieces) load_piece(wa, pc + 2);
+                store_piece(wb, pc + 1);
+                if (pc + 3 < kQPieces) load_piece(wb, pc + 3);
             }
             ptx::cp_async_wait<0>();
             ptx::tmem_st_wait();
