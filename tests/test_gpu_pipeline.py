@@ -45,11 +45,17 @@ def host_out(x):
             torch.empty((B, T, 128), dtype=torch.float32).pin_memory())
 
 
+# 16 tokens a sequence: the indexer's token groups inside the pipelined step
+CUSTOM = {"csa_b2t16_ctx20k_k128": synth.custom("csa", B=2, T=16, ncap=5000, k=128, ctx=20000,
+                                               name="csa_b2t16_ctx20k_k128")}
+
+
 @pytest.mark.parametrize("name,depth", [("csa_b1_ctx1k_k64", 2), ("csa_b8_ctx16k32k_k512", 2),
-                                        ("csa_b8_ctx16k32k_k512", 3), ("csa_b4t4_ctx1m_k2048", 4)])
+                                        ("csa_b8_ctx16k32k_k512", 3), ("csa_b4t4_ctx1m_k2048", 4),
+                                        ("csa_b2t16_ctx20k_k128", 2)])
 def test_pipeline_matches_decode_step(cuda_lib, name, depth):
     csd = cuda_lib
-    x = synth.generate(name, seed=0, device="cuda")
+    x = synth.generate(CUSTOM.get(name, name), seed=0, device="cuda")
     comp = csd.cache_desc(x.comp, x.wl.ncap, x.seq_stride)
     ins = [step_inputs(x, j) for j in range(STEPS)]
     want = [expected(csd, x, comp, i) for i in ins]
