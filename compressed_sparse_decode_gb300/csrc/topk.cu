@@ -2,10 +2,12 @@
 // ("DSV4 Audit", section B2; "ROADMAP -- Stage E", section E7: top-k with
 // warp-level reductions and no global lock).
 //
-// Two kernels. The 8-bit radix select below (topk_radix8_kernel) serves every
-// row whose keys fit in the shared memory of one cluster (up to 360448
-// entries); the 11-bit cluster kernel that follows serves longer rows, its
-// keys read from global memory in every pass when they do not fit.
+// Three kernels. Rows of up to 32768 entries take one CTA each with the keys
+// in registers (topk_row_kernel, at the end); longer rows whose keys fit in
+// the shared memory of one cluster (up to 360448 entries) take the 8-bit
+// radix select over a cluster (topk_radix8_kernel); the 11-bit cluster kernel
+// described next serves longer rows still, its keys read from global memory
+// in every pass when they do not fit.
 //
 // Cluster kernel: one row (query token) per cluster of 8 CTAs of 512 threads
 // (1024 for rows above 64K entries); CTA rank c owns the slice
@@ -601,6 +603,300 @@ topk_radix8_kernel(const float *__restrict__ logits, const int32_t *__restrict__
     if (crank == 0 && tid == 0) cnt_out[r] = k;
 }
 
+// ------------------------------------------------------------------ one CTA per row
+//
+// Rows of up to 32768 entries: one CTA of 1024 threads per row, the row's keys
+// in registers (KPT a thread), so that no step needs a cluster barrier: at
+// these sizes the barriers and remote round trips of the cluster kernels above
+// cost more than their passes' work. Warp w holds the contiguous chunk
+// [w * 32 * KPT, (w + 1) * 32 * KPT) of the row, loaded as coalesced 16-byte
+// groups: lane L holds the chunk's groups j * 32 + L (j < KPT / 4).
+//
+// The radix select takes two 16-bit digits, each counted into a 65536-bin
+// shared-memory histogram (two 16-bit counters a word: a row has at most 32768
+// keys): one predicated shared-memory add per key and pass, no per-key
+// branch. A descending scan over the histogram (thread t owns 64 bins, thread
+// order = descending bin order; one block scan of the per-thread totals) finds
+// the bin of the `need`-th largest counted key. The compaction gives every kept
+// key its slot in closed form, walking the row in index order (warp, group j,
+// lane, element): per group a warp scan of byte-packed kept counts, on top of
+// the kept counts of the warps before. Keys equal to K* are kept up to the
+// budget, lowest index first: when the budget cuts them (ties), the index of
+// the last one kept is found first, in the same index order.
+struct RowShared {
+    int wsum[32];
+    int wtot[32];
+    uint32_t sel;  // the selected bin of the current pass
+    int rem;       // keys still needed from that bin
+    int cnt;       // keys in that bin
+    int ithr;      // index of the last key == K* kept
+    int nlist;     // keys listed for the second digit (short-list path)
+};
+constexpr int kRowMaxList = 256;  // second digit by ranking a list of at most this many keys
+constexpr int kRowThreads = 1024;
+constexpr size_t kRowHistBytes = 65536 * 2;  // 65536 16-bit counters
+
+__device__ __forceinline__ void red_shared_add_if(uint32_t saddr, uint32_t v, bool c) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q red.shared.add.u32 [%0], %1;\n\t}" ::"r"(saddr), "r"(v),
+        "r"((uint32_t)c)
+        : "memory");
+}
+__device__ __forceinline__ void st_global_if(int32_t *p, int32_t v, bool c) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q st.global.b32 [%0], %1;\n\t}" ::"l"(p), "r"(v),
+                 "r"((uint32_t)c)
+                 : "memory");
+}
+__device__ __forceinline__ uint32_t byte_sum(uint32_t x) { return (x & 0xFFu) + ((x >> 8) & 0xFFu) + ((x >> 16) & 0xFFu) + (x >> 24); }
+
+// Inclusive warp scan of four byte counters packed in a word (each column's
+// sum stays below 256).
+__device__ __forceinline__ uint32_t warp_scan_bytes(uint32_t v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+    }
+    return v;
+}
+
+// (Not inlined: called twice with the 32 keys a thread live in registers, it
+// kept the kernel from spilling.)
+// The bin of the `need`-th largest counted key (1 <= need <= counted keys):
+// s.sel, s.rem (keys still needed from it), s.cnt (keys in it). Every thread
+// calls it; the histogram is complete and visible on entry, s.* on return.
+__device__ __noinline__ void select_bin(const uint32_t *h32, int need, RowShared &s, int tid, int lane, int warp) {
+    const int u = kRowThreads - 1 - tid;  // thread order = descending bins
+    const uint4 *w4 = reinterpret_cast<const uint4 *>(h32 + 32 * u);
+    uint32_t acc = 0u;  // per half: at most 32768 counts, so the low half never carries
+#pragma unroll 2
+    for (int i = 0; i < 8; ++i) {
+        const uint4 v = w4[(i + lane) & 7];  // rotated: lanes of a quarter warp read distinct banks
+        acc += v.x + v.y + v.z + v.w;
+    }
+    const int total = (int)((acc & 0xFFFFu) + (acc >> 16));
+    int incl = total;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) s.wsum[warp] = incl;
+    __syncthreads();
+    const int base = (int)__reduce_add_sync(0xffffffffu, lane < warp ? (unsigned)s.wsum[lane] : 0u);
+    const int cum = base + incl - total;
+    // the warp whose thread holds it walks that thread's 64 bins, two a lane
+    // (lane L: bins 64 u' + 63 - 2 L, 64 u' + 62 - 2 L, largest first)
+    const unsigned own = __ballot_sync(0xffffffffu, total > 0 && cum < need && need <= cum + total);
+    if (own) {  // uniform over the warp
+        const int src = __ffs(own) - 1;
+        const int uo = kRowThreads - 1 - (warp * 32 + src);
+        const int c0 = __shfl_sync(0xffffffffu, cum, src);
+        const uint32_t x = h32[32 * uo + 31 - lane];
+        const int hi = (int)(x >> 16), lo = (int)(x & 0xFFFFu);
+        int in = hi + lo;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, in, o);
+            if (lane >= o) in += t;
+        }
+        const int before = c0 + in - hi - lo;
+        if (before < need && need <= before + hi + lo) {
+            const bool top = need <= before + hi;
+            s.sel = (uint32_t)(64 * uo + 63 - 2 * lane - (top ? 0 : 1));
+            s.rem = need - (top ? before : before + hi);
+            s.cnt = top ? hi : lo;
+        }
+    }
+    __syncthreads();
+}
+
+template <int KPT>
+__global__ void __launch_bounds__(kRowThreads, 1)
+topk_row_kernel(const float *__restrict__ logits, const int32_t *__restrict__ q_pos,
+                const int32_t *__restrict__ n_comp, int T, int Ncap, int m, int k, int32_t *__restrict__ idx_out,
+                int32_t *__restrict__ cnt_out) {
+    static_assert(KPT % 4 == 0 && KPT <= 32, "keys a thread: groups of 4, one bit each in a 32-bit mask");
+    constexpr int G = KPT / 4;
+    extern __shared__ __align__(16) uint32_t h32[];  // the histogram, kRowHistBytes
+    __shared__ RowShared s;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint4 *h4 = reinterpret_cast<uint4 *>(h32);
+    const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int i = 0; i < (int)(kRowHistBytes / 16 / kRowThreads); ++i) h4[i * kRowThreads + tid] = zero4;
+    if (tid == 0) s.nlist = 0;
+    ptx::griddep_wait();  // the logits (previous kernel in the stream) are complete and visible
+    const int r = blockIdx.x;
+    const int b = r / T;
+    const float *row = logits + (size_t)r * Ncap;
+    int32_t *out = idx_out + (size_t)r * k;
+    const int nv = visible_entries(__ldg(q_pos + r), m, __ldg(n_comp + b), Ncap);
+
+    if (nv <= k) {
+        // every visible entry is selected
+        for (int i = tid; i < k; i += kRowThreads) out[i] = i < nv ? i : -1;
+        if (tid == 0) cnt_out[r] = nv;
+        return;
+    }
+
+    const int chunk = warp * 32 * KPT;
+    auto first = [&](int j) { return chunk + 4 * (j * 32 + lane); };  // first entry of group j
+    uint32_t key[KPT];
+    if ((Ncap & 3) == 0) {
+        // rows of a multiple of 4 entries: every group inside the row is a whole, aligned float4
+        const uint64_t policy = ptx::l2_policy_evict_first();  // the logits are read once
+        uint4 w[G];
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            w[j] = zero4;
+            if (first(j) < nv) w[j] = ptx::ldg_v4_policy(row + first(j), policy);
+        }
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            const uint32_t v[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) key[4 * j + e] = order_key(__uint_as_float(v[e]));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = first(j) + e;
+                key[4 * j + e] = i < nv ? order_key(__ldg(row + i)) : 0u;
+            }
+    }
+    if (first(G - 1) + 3 >= nv) {
+        // the row's visible end falls in this thread's groups: entries past it become key 0
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) key[4 * j + e] = first(j) + e < nv ? key[4 * j + e] : 0u;
+    }
+    // (entries past the visible range hold key 0, below every real key and
+    // counted in neither pass; K* is a real key)
+    __syncthreads();  // the zeroed histogram
+
+    const uint32_t hbase = ptx::smem_u32(h32);
+    // ---- pass 1: the top 16 bits (bin = key >> 16: word key >> 17, half bit 16)
+#pragma unroll
+    for (int i = 0; i < KPT; ++i)
+        red_shared_add_if(hbase + ((key[i] >> 17) << 2), 1u << ((key[i] >> 12) & 16u), key[i] != 0u);
+    __syncthreads();
+    select_bin(h32, k, s, tid, lane, warp);
+    const uint32_t hi16 = s.sel;
+    const int need = s.rem;
+    if (s.cnt <= kRowMaxList) {  // uniform
+        // ---- pass 2, short list: the few keys of that bin, ranked by their low
+        // 16 bits (the histogram's memory is free from here on)
+        const int n = s.cnt;
+#pragma unroll
+        for (int i = 0; i < KPT; ++i)
+            if (key[i] != 0u && (key[i] >> 16) == hi16) h32[atomicAdd(&s.nlist, 1)] = key[i] & 0xFFFFu;
+        __syncthreads();
+        if (tid < n) {
+            const uint32_t v = h32[tid];
+            int gt = 0, ge = 0;
+            for (int i = 0; i < n; ++i) {
+                const uint32_t x = h32[i];
+                gt += x > v ? 1 : 0;
+                ge += x >= v ? 1 : 0;
+            }
+            if (gt < need && need <= ge) {  // every thread holding the selected value writes the same
+                s.sel = v;
+                s.rem = need - gt;
+                s.cnt = ge - gt;
+            }
+        }
+        __syncthreads();
+    } else {
+#pragma unroll
+        for (int i = 0; i < (int)(kRowHistBytes / 16 / kRowThreads); ++i) h4[i * kRowThreads + tid] = zero4;
+        __syncthreads();
+        // ---- pass 2: the low 16 bits of the keys in that bin
+#pragma unroll
+        for (int i = 0; i < KPT; ++i)
+            red_shared_add_if(hbase + ((key[i] & 0xFFFFu) >> 1 << 2), 1u << ((key[i] & 1u) << 4),
+                              key[i] != 0u && (key[i] >> 16) == hi16);
+        __syncthreads();
+        select_bin(h32, need, s, tid, lane, warp);
+    }
+    const uint32_t kstar = (hi16 << 16) | s.sel;
+    const int budget = s.rem;  // keys == K* kept, of s.cnt
+    // keep: bit 4 j + e for the key of group j, element e
+    uint32_t keep = 0u;
+    if (budget == s.cnt) {  // uniform: every key == K* is kept
+#pragma unroll
+        for (int i = 0; i < KPT; ++i) keep |= (key[i] >= kstar ? 1u : 0u) << i;
+    } else {
+        // ---- the budget cuts the keys == K* (ties): find the index of the last one kept
+        uint32_t gtm = 0u, eqm = 0u;
+#pragma unroll
+        for (int i = 0; i < KPT; ++i) {
+            gtm |= (key[i] > kstar ? 1u : 0u) << i;
+            eqm |= (key[i] == kstar ? 1u : 0u) << i;
+        }
+        uint32_t pk[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < G; ++j) pk[j >> 2] |= (uint32_t)__popc((eqm >> (4 * j)) & 0xFu) << (8 * (j & 3));
+        const uint32_t in0 = warp_scan_bytes(pk[0], lane), in1 = warp_scan_bytes(pk[1], lane);
+        const uint32_t t0 = __shfl_sync(0xffffffffu, in0, 31), t1 = __shfl_sync(0xffffffffu, in1, 31);
+        if (lane == 0) s.wtot[warp] = (int)(byte_sum(t0) + byte_sum(t1));
+        __syncthreads();
+        const int before = (int)__reduce_add_sync(0xffffffffu, lane < warp ? (unsigned)s.wtot[lane] : 0u);
+        if (before < budget && budget <= before + s.wtot[warp]) {  // uniform over the warp
+            int left = budget - before;  // the left-th key == K* of this warp, in index order
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                const uint32_t tj = ((j < 4 ? t0 : t1) >> (8 * (j & 3))) & 0xFFu;
+                const uint32_t ij = ((j < 4 ? in0 : in1) >> (8 * (j & 3))) & 0xFFu;
+                const uint32_t nib = (eqm >> (4 * j)) & 0xFu;
+                const int ex = (int)ij - __popc(nib);
+                if (left > 0 && left <= (int)tj && ex < left && left <= (int)ij) {
+                    // this lane holds it: the (left - ex)-th set bit of its group
+                    int c = left - ex;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if ((nib >> e) & 1u) {
+                            if (--c == 0) s.ithr = first(j) + e;
+                        }
+                    }
+                }
+                left -= left > 0 ? (int)tj : 0;
+            }
+        }
+        __syncthreads();
+        const int ithr = s.ithr;
+        keep = gtm;
+#pragma unroll
+        for (int i = 0; i < KPT; ++i) keep |= ((eqm >> i) & 1u) && first(i >> 2) + (i & 3) <= ithr ? 1u << i : 0u;
+    }
+
+    // ---- compaction: keys > K*, and keys == K* up to the budget
+    uint32_t pk[2] = {0u, 0u};  // kept keys per group, bytes (groups 0-3, 4-7)
+#pragma unroll
+    for (int j = 0; j < G; ++j) pk[j >> 2] |= (uint32_t)__popc((keep >> (4 * j)) & 0xFu) << (8 * (j & 3));
+    const uint32_t in0 = warp_scan_bytes(pk[0], lane), in1 = G > 4 ? warp_scan_bytes(pk[1], lane) : 0u;
+    const uint32_t t0 = __shfl_sync(0xffffffffu, in0, 31), t1 = __shfl_sync(0xffffffffu, in1, 31);
+    if (lane == 0) s.wtot[warp] = (int)(byte_sum(t0) + byte_sum(t1));
+    __syncthreads();
+    const int base = (int)__reduce_add_sync(0xffffffffu, lane < warp ? (unsigned)s.wtot[lane] : 0u);
+    const uint32_t ex0 = in0 - pk[0], ex1 = in1 - pk[1];  // kept keys of the lanes before, per group (bytes)
+    // every kept key (about k / 1024 a thread): its slot = the warps before + the
+    // groups before + the lanes before in its group + its group's keys before it
+    for (uint32_t mk = keep; mk != 0u; mk &= mk - 1u) {
+        const int bit = __ffs(mk) - 1, j = bit >> 2;
+        const uint32_t sh = 8u * (uint32_t)(j & 3), below = (1u << sh) - 1u;
+        const int groups_before = j < 4 ? (int)__dp4a(t0 & below, 0x01010101u, 0u)
+                                        : (int)(__dp4a(t0, 0x01010101u, 0u) + __dp4a(t1 & below, 0x01010101u, 0u));
+        const int lanes_before = (int)(((j < 4 ? ex0 : ex1) >> sh) & 0xFFu);
+        const int pos = base + groups_before + lanes_before + __popc(keep & (0xFu << (4 * j)) & ((1u << bit) - 1u));
+        if (pos < k) out[pos] = first(j) + (bit & 3);
+    }
+    if (tid == 0) cnt_out[r] = k;
+}
+
 }  // namespace
 
 size_t topk_workspace_bytes(int, int, int, int) { return 0; }
@@ -722,10 +1018,36 @@ cudaError_t launch_r8(const float *logits, const int32_t *q_pos, const int32_t *
     return cudaGetLastError();
 }
 
+template <int KPT>
+cudaError_t launch_row(const float *logits, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap, int m,
+                       int k, int32_t *idx_out, int32_t *cnt_out, cudaStream_t stream) {
+    // the caller checks Ncap <= kRowThreads * KPT
+    cudaError_t e = set_max_dynamic_smem_once(reinterpret_cast<const void *>(topk_row_kernel<KPT>), (int)kRowHistBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(B * T);
+    cfg.blockDim = dim3(kRowThreads);
+    cfg.dynamicSmemBytes = kRowHistBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the indexer ends
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    count_launch();
+    e = cudaLaunchKernelEx(&cfg, topk_row_kernel<KPT>, logits, q_pos, n_comp, T, Ncap, m, k, idx_out, cnt_out);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 cudaError_t launch_topk(const float *logits, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap,
                         int m, int k, int32_t *idx_out, int32_t *cnt_out, void *, size_t, cudaStream_t stream) {
-    // Rows whose keys fit in the shared memory of a cluster (up to 8 x 1024
-    // threads x 44 keys): the 8-bit radix select, 256 threads a CTA up to
+    // Rows of up to 32768 entries: one CTA a row, keys in registers (8 a
+    // thread up to 8192 entries, 32 above).
+    if (Ncap <= kRowThreads * 8) return launch_row<8>(logits, q_pos, n_comp, B, T, Ncap, m, k, idx_out, cnt_out, stream);
+    if (Ncap <= kRowThreads * 32) return launch_row<32>(logits, q_pos, n_comp, B, T, Ncap, m, k, idx_out, cnt_out, stream);
+    // Longer rows whose keys fit in the shared memory of a cluster (up to 8 x
+    // 1024 threads x 44 keys): the 8-bit radix select, 256 threads a CTA up to
     // 65536 entries, 1024 above. Measured against the 11-bit cluster kernel
     // (events around 20 calls on rotating inputs): 8.1 against 14.2 us for
     // 256-entry rows, 13.6 against 14.3 us for 8192, 18.8 against 19.9 us for

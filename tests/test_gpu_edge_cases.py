@@ -114,9 +114,10 @@ def test_paged_cache_matches_contiguous_and_oracle(cuda_lib):
         assert np.array_equal(kv.cpu().numpy()[r][:okc[r]], okv[r][:okc[r]])
 
 
-# 5000: 512-thread CTAs; 70001 (ragged, scalar loads) and 131076 (16-byte
-# loads): rows long enough for the 1024-thread CTAs
-@pytest.mark.parametrize("ncap", [5000, 70001, 131076])
+# 5000, 8192 (8 keys a thread), 20001 (ragged rows: scalar loads) and 32768
+# (32 keys a thread): one CTA a row; 70001 (ragged) and 131076 (16-byte
+# loads): the 8-bit cluster select with 1024-thread CTAs
+@pytest.mark.parametrize("ncap", [5000, 8192, 20001, 32768, 70001, 131076])
 def test_topk_heavy_ties_and_extremes(cuda_lib, ncap):
     rng = np.random.default_rng(0)
     B, T = 3, 2
