@@ -711,11 +711,25 @@ __device__ __noinline__ void select_bin(const uint32_t *h32, int need, RowShared
     __syncthreads();
 }
 
-template <int KPT>
+// What one CTA of topk_row_kernel selects from: a whole row; one slice of
+// kRowThreads * KPT entries of a longer row (first stage: the slice's top k,
+// indices into the row with their order-preserving keys, unused slots -1 and
+// key 0, and the slice's k-th key); or the candidates of all S slices of a
+// row, S * k of them (second stage: the row's top k among them).
+enum RowMode { kModeWhole = 0, kModeSlice = 1, kModeMerge = 2 };
+
+// The two-stage scratch of `slots` = rows * S candidate lists of k: indices
+// int32 [slots][k], then (16-byte aligned) keys uint32 [slots][k], then the
+// slices' k-th keys uint32 [slots].
+__host__ __device__ __forceinline__ size_t cand_keys_offset(size_t slots, int k) {
+    return (slots * (size_t)k + 3) & ~(size_t)3;
+}
+
+template <int KPT, int kMode>
 __global__ void __launch_bounds__(kRowThreads, 1)
 topk_row_kernel(const float *__restrict__ logits, const int32_t *__restrict__ q_pos,
-                const int32_t *__restrict__ n_comp, int T, int Ncap, int m, int k, int32_t *__restrict__ idx_out,
-                int32_t *__restrict__ cnt_out) {
+                const int32_t *__restrict__ n_comp, int T, int Ncap, int m, int k, int S, int32_t *__restrict__ cand,
+                int32_t *__restrict__ idx_out, int32_t *__restrict__ cnt_out) {
     static_assert(KPT % 4 == 0 && KPT <= 32, "keys a thread: groups of 4, one bit each in a 32-bit mask");
     constexpr int G = KPT / 4;
     extern __shared__ __align__(16) uint32_t h32[];  // the histogram, kRowHistBytes
@@ -726,63 +740,123 @@ topk_row_kernel(const float *__restrict__ logits, const int32_t *__restrict__ q_
 #pragma unroll
     for (int i = 0; i < (int)(kRowHistBytes / 16 / kRowThreads); ++i) h4[i * kRowThreads + tid] = zero4;
     if (tid == 0) s.nlist = 0;
-    ptx::griddep_wait();  // the logits (previous kernel in the stream) are complete and visible
-    const int r = blockIdx.x;
+    ptx::griddep_wait();  // the logits (and candidates) of the previous kernel in the stream are complete and visible
+    const int r = kMode == kModeSlice ? (int)blockIdx.x / S : (int)blockIdx.x;
     const int b = r / T;
-    const float *row = logits + (size_t)r * Ncap;
-    int32_t *out = idx_out + (size_t)r * k;
+    const float *lrow = logits + (size_t)r * Ncap;
     const int nv = visible_entries(__ldg(q_pos + r), m, __ldg(n_comp + b), Ncap);
+    // this CTA's entries [0, n): row entry base + i (whole row, slice) or the
+    // row entry named by candidate i (merge)
+    int n = nv, base = 0;
+    int32_t *out = idx_out + (size_t)r * k;
+    const size_t slots = kMode == kModeSlice ? gridDim.x : (size_t)gridDim.x * S;  // rows * S
+    uint32_t *const ckeys = reinterpret_cast<uint32_t *>(cand + cand_keys_offset(slots, k));
+    uint32_t *const cthr = ckeys + slots * k;
+    const int32_t *crow = cand + (size_t)r * S * k;
+    uint32_t *kout = nullptr;  // slice: the candidates' keys
+    if (kMode == kModeSlice) {
+        base = ((int)blockIdx.x - r * S) * kRowThreads * KPT;
+        n = min(max(nv - base, 0), kRowThreads * KPT);
+        out = cand + (size_t)blockIdx.x * k;
+        kout = ckeys + (size_t)blockIdx.x * k;
+    } else if (kMode == kModeMerge) {
+        n = S * k;
+    }
 
-    if (nv <= k) {
-        // every visible entry is selected
-        for (int i = tid; i < k; i += kRowThreads) out[i] = i < nv ? i : -1;
-        if (tid == 0) cnt_out[r] = nv;
+    if ((kMode == kModeSlice ? n : nv) <= k) {
+        // every visible entry (of the slice) is selected
+        const int all = kMode == kModeSlice ? n : nv;
+        for (int i = tid; i < k; i += kRowThreads) {
+            out[i] = i < all ? base + i : -1;
+            if (kMode == kModeSlice) kout[i] = i < all ? order_key(__ldg(lrow + base + i)) : 0u;
+        }
+        if (kMode != kModeSlice && tid == 0) cnt_out[r] = nv;
+        if (kMode == kModeSlice && tid == 0) cthr[blockIdx.x] = 0u;  // no k-th key: no bound on the row's
         return;
     }
 
     const int chunk = warp * 32 * KPT;
     auto first = [&](int j) { return chunk + 4 * (j * 32 + lane); };  // first entry of group j
     uint32_t key[KPT];
-    if ((Ncap & 3) == 0) {
-        // rows of a multiple of 4 entries: every group inside the row is a whole, aligned float4
-        const uint64_t policy = ptx::l2_policy_evict_first();  // the logits are read once
-        uint4 w[G];
+    // Merge: the candidates' indices, copied into shared memory behind the
+    // histogram while the selection runs (read back for the kept keys only).
+    int32_t *const sidx = reinterpret_cast<int32_t *>(h32 + kRowHistBytes / 4);
+    const bool idx_in_smem = kMode == kModeMerge && KPT <= 16 && (n & 3) == 0;
+    if (idx_in_smem) {
+        const uint64_t policy = ptx::l2_policy_evict_first();
+        for (int c = tid; c < n / 4; c += kRowThreads) ptx::cp_async_16_hint(sidx + 4 * c, crow + 4 * c, policy);
+        ptx::cp_async_commit();
+    }
+    if (kMode == kModeMerge) {
+        // the candidates' keys (unused slots hold key 0)
+        const uint32_t *krow = ckeys + (size_t)r * S * k;
+        if ((n & 3) == 0) {  // with k % 4 == 0 every row of keys is 16-byte aligned
 #pragma unroll
-        for (int j = 0; j < G; ++j) {
-            w[j] = zero4;
-            if (first(j) < nv) w[j] = ptx::ldg_v4_policy(row + first(j), policy);
-        }
+            for (int j = 0; j < G; ++j) {
+                uint4 v = zero4;
+                if (first(j) < n) v = __ldg(reinterpret_cast<const uint4 *>(krow + first(j)));
+                key[4 * j] = v.x;
+                key[4 * j + 1] = v.y;
+                key[4 * j + 2] = v.z;
+                key[4 * j + 3] = v.w;
+            }
+        } else {
 #pragma unroll
-        for (int j = 0; j < G; ++j) {
-            const uint32_t v[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) key[4 * j + e] = order_key(__uint_as_float(v[e]));
+            for (int i = 0; i < KPT; ++i) {
+                const int e = first(i >> 2) + (i & 3);
+                key[i] = e < n ? __ldg(krow + e) : 0u;
+            }
         }
     } else {
+        const float *row = lrow + base;
+        if ((Ncap & 3) == 0) {
+            // rows of a multiple of 4 entries: every group inside the row is a whole, aligned float4
+            const uint64_t policy = ptx::l2_policy_evict_first();  // the logits are read once
+            uint4 w[G];
 #pragma unroll
-        for (int j = 0; j < G; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = first(j) + e;
-                key[4 * j + e] = i < nv ? order_key(__ldg(row + i)) : 0u;
+            for (int j = 0; j < G; ++j) {
+                w[j] = zero4;
+                if (first(j) < n) w[j] = ptx::ldg_v4_policy(row + first(j), policy);
             }
-    }
-    if (first(G - 1) + 3 >= nv) {
-        // the row's visible end falls in this thread's groups: entries past it become key 0
 #pragma unroll
-        for (int j = 0; j < G; ++j)
+            for (int j = 0; j < G; ++j) {
+                const uint32_t v[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) key[4 * j + e] = first(j) + e < nv ? key[4 * j + e] : 0u;
+                for (int e = 0; e < 4; ++e) key[4 * j + e] = order_key(__uint_as_float(v[e]));
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = first(j) + e;
+                    key[4 * j + e] = i < n ? order_key(__ldg(row + i)) : 0u;
+                }
+        }
+        if (first(G - 1) + 3 >= n) {
+            // the visible end falls in this thread's groups: entries past it become key 0
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) key[4 * j + e] = first(j) + e < n ? key[4 * j + e] : 0u;
+        }
     }
     // (entries past the visible range hold key 0, below every real key and
     // counted in neither pass; K* is a real key)
     __syncthreads();  // the zeroed histogram
 
+    // Keys below `floor` are counted nowhere (and so never selected). Merge:
+    // the largest of the slices' k-th keys, which the row's k-th key is not
+    // below (that slice alone holds k keys at or above it); it drops most of
+    // the candidates, which crowd into few bins of the first digit.
+    uint32_t floor = 1u;
+    if (kMode == kModeMerge)
+        floor = max(1u, __reduce_max_sync(0xffffffffu, lane < S ? __ldg(cthr + (size_t)r * S + lane) : 0u));
     const uint32_t hbase = ptx::smem_u32(h32);
     // ---- pass 1: the top 16 bits (bin = key >> 16: word key >> 17, half bit 16)
 #pragma unroll
     for (int i = 0; i < KPT; ++i)
-        red_shared_add_if(hbase + ((key[i] >> 17) << 2), 1u << ((key[i] >> 12) & 16u), key[i] != 0u);
+        red_shared_add_if(hbase + ((key[i] >> 17) << 2), 1u << ((key[i] >> 12) & 16u), key[i] >= floor);
     __syncthreads();
     select_bin(h32, k, s, tid, lane, warp);
     const uint32_t hi16 = s.sel;
@@ -793,7 +867,7 @@ topk_row_kernel(const float *__restrict__ logits, const int32_t *__restrict__ q_
         const int n = s.cnt;
 #pragma unroll
         for (int i = 0; i < KPT; ++i)
-            if (key[i] != 0u && (key[i] >> 16) == hi16) h32[atomicAdd(&s.nlist, 1)] = key[i] & 0xFFFFu;
+            if (key[i] >= floor && (key[i] >> 16) == hi16) h32[atomicAdd(&s.nlist, 1)] = key[i] & 0xFFFFu;
         __syncthreads();
         if (tid < n) {
             const uint32_t v = h32[tid];
@@ -818,12 +892,20 @@ topk_row_kernel(const float *__restrict__ logits, const int32_t *__restrict__ q_
 #pragma unroll
         for (int i = 0; i < KPT; ++i)
             red_shared_add_if(hbase + ((key[i] & 0xFFFFu) >> 1 << 2), 1u << ((key[i] & 1u) << 4),
-                              key[i] != 0u && (key[i] >> 16) == hi16);
+                              key[i] >= floor && (key[i] >> 16) == hi16);
         __syncthreads();
         select_bin(h32, need, s, tid, lane, warp);
     }
     const uint32_t kstar = (hi16 << 16) | s.sel;
     const int budget = s.rem;  // keys == K* kept, of s.cnt
+    if (kMode == kModeSlice && tid == 0) cthr[blockIdx.x] = kstar;  // the slice's k-th key
+    if (kMode == kModeSlice) {
+        // the keys into the (now unused) histogram memory, by entry, for the
+        // kept ones' candidate keys (each thread reads back only its own)
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+            *reinterpret_cast<uint4 *>(h32 + first(j)) = make_uint4(key[4 * j], key[4 * j + 1], key[4 * j + 2], key[4 * j + 3]);
+    }
     // keep: bit 4 j + e for the key of group j, element e
     uint32_t keep = 0u;
     if (budget == s.cnt) {  // uniform: every key == K* is kept
@@ -873,6 +955,8 @@ topk_row_kernel(const float *__restrict__ logits, const int32_t *__restrict__ q_
         for (int i = 0; i < KPT; ++i) keep |= ((eqm >> i) & 1u) && first(i >> 2) + (i & 3) <= ithr ? 1u << i : 0u;
     }
 
+    if (idx_in_smem) ptx::cp_async_wait<0>();  // made visible to the block by the barrier below
+
     // ---- compaction: keys > K*, and keys == K* up to the budget
     uint32_t pk[2] = {0u, 0u};  // kept keys per group, bytes (groups 0-3, 4-7)
 #pragma unroll
@@ -881,7 +965,7 @@ topk_row_kernel(const float *__restrict__ logits, const int32_t *__restrict__ q_
     const uint32_t t0 = __shfl_sync(0xffffffffu, in0, 31), t1 = __shfl_sync(0xffffffffu, in1, 31);
     if (lane == 0) s.wtot[warp] = (int)(byte_sum(t0) + byte_sum(t1));
     __syncthreads();
-    const int base = (int)__reduce_add_sync(0xffffffffu, lane < warp ? (unsigned)s.wtot[lane] : 0u);
+    const int wbase = (int)__reduce_add_sync(0xffffffffu, lane < warp ? (unsigned)s.wtot[lane] : 0u);
     const uint32_t ex0 = in0 - pk[0], ex1 = in1 - pk[1];  // kept keys of the lanes before, per group (bytes)
     // every kept key (about k / 1024 a thread): its slot = the warps before + the
     // groups before + the lanes before in its group + its group's keys before it
@@ -891,17 +975,16 @@ topk_row_kernel(const float *__restrict__ logits, const int32_t *__restrict__ q_
         const int groups_before = j < 4 ? (int)__dp4a(t0 & below, 0x01010101u, 0u)
                                         : (int)(__dp4a(t0, 0x01010101u, 0u) + __dp4a(t1 & below, 0x01010101u, 0u));
         const int lanes_before = (int)(((j < 4 ? ex0 : ex1) >> sh) & 0xFFu);
-        const int pos = base + groups_before + lanes_before + __popc(keep & (0xFu << (4 * j)) & ((1u << bit) - 1u));
-        if (pos < k) out[pos] = first(j) + (bit & 3);
+        const int pos = wbase + groups_before + lanes_before + __popc(keep & (0xFu << (4 * j)) & ((1u << bit) - 1u));
+        const int i = first(j) + (bit & 3);
+        if (pos < k) {
+            out[pos] = kMode == kModeMerge ? (idx_in_smem ? sidx[i] : __ldg(crow + i)) : base + i;
+            if (kMode == kModeSlice) kout[pos] = h32[i];
+        }
     }
-    if (tid == 0) cnt_out[r] = k;
+    if (kMode != kModeSlice && tid == 0) cnt_out[r] = k;
 }
 
-}  // namespace
-
-size_t topk_workspace_bytes(int, int, int, int) { return 0; }
-
-namespace {
 
 template <int kThreads>
 cudaError_t launch_t(const float *logits, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap, int m,
@@ -1018,34 +1101,86 @@ cudaError_t launch_r8(const float *logits, const int32_t *q_pos, const int32_t *
     return cudaGetLastError();
 }
 
-template <int KPT>
-cudaError_t launch_row(const float *logits, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap, int m,
-                       int k, int32_t *idx_out, int32_t *cnt_out, cudaStream_t stream) {
-    // the caller checks Ncap <= kRowThreads * KPT
-    cudaError_t e = set_max_dynamic_smem_once(reinterpret_cast<const void *>(topk_row_kernel<KPT>), (int)kRowHistBytes);
+namespace {
+
+template <int KPT, int kMode>
+cudaError_t launch_row(const float *logits, const int32_t *q_pos, const int32_t *n_comp, int rows, int ctas, int T,
+                       int Ncap, int m, int k, int S, int32_t *cand, int32_t *idx_out, int32_t *cnt_out,
+                       cudaStream_t stream) {
+    const void *kernel = reinterpret_cast<const void *>(topk_row_kernel<KPT, kMode>);
+    // merge with up to 16384 candidates: their indices after the histogram
+    const size_t smem = kRowHistBytes + (kMode == kModeMerge && KPT <= 16 ? sizeof(int32_t) * kRowThreads * KPT : 0);
+    cudaError_t e = set_max_dynamic_smem_once(kernel, (int)smem);
     if (e != cudaSuccess) return e;
+    (void)rows;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(B * T);
+    cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(kRowThreads);
-    cfg.dynamicSmemBytes = kRowHistBytes;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the indexer ends
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before its predecessor ends
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     count_launch();
-    e = cudaLaunchKernelEx(&cfg, topk_row_kernel<KPT>, logits, q_pos, n_comp, T, Ncap, m, k, idx_out, cnt_out);
+    e = cudaLaunchKernelEx(&cfg, topk_row_kernel<KPT, kMode>, logits, q_pos, n_comp, T, Ncap, m, k, S, cand, idx_out,
+                           cnt_out);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
+// Rows longer than one CTA holds, cut into S slices of kRowSlice entries:
+// the slices' candidates (S * k of them) must fit one CTA too.
+constexpr int kRowSlice = kRowThreads * 32;
+int row_slices(int Ncap, int k) {
+    if (Ncap <= kRowSlice) return 0;
+    const int S = (Ncap + kRowSlice - 1) / kRowSlice;
+    return (int64_t)S * k <= kRowSlice ? S : 0;
+}
+
+}  // namespace
+
+size_t topk_workspace_bytes(int B, int T, int Ncap, int k) {
+    // two-stage rows: the slices' candidates (indices, keys) and k-th keys
+    if (B < 1 || T < 1 || k < 1) return 0;
+    const int S = row_slices(Ncap, k);
+    if (!S) return 0;
+    const size_t slots = (size_t)B * T * S;
+    return sizeof(uint32_t) * (cand_keys_offset(slots, k) + slots * k + slots);
+}
+
 cudaError_t launch_topk(const float *logits, const int32_t *q_pos, const int32_t *n_comp, int B, int T, int Ncap,
-                        int m, int k, int32_t *idx_out, int32_t *cnt_out, void *, size_t, cudaStream_t stream) {
-    // Rows of up to 32768 entries: one CTA a row, keys in registers (8 a
-    // thread up to 8192 entries, 32 above).
-    if (Ncap <= kRowThreads * 8) return launch_row<8>(logits, q_pos, n_comp, B, T, Ncap, m, k, idx_out, cnt_out, stream);
-    if (Ncap <= kRowThreads * 32) return launch_row<32>(logits, q_pos, n_comp, B, T, Ncap, m, k, idx_out, cnt_out, stream);
+                        int m, int k, int32_t *idx_out, int32_t *cnt_out, void *workspace, size_t,
+                        cudaStream_t stream) {
+    // Rows of up to 32768 entries: one CTA a row, keys in registers (8, 16 or
+    // 32 a thread).
+    const int rows = B * T;
+    if (Ncap <= kRowThreads * 8)
+        return launch_row<8, kModeWhole>(logits, q_pos, n_comp, rows, rows, T, Ncap, m, k, 0, nullptr, idx_out, cnt_out,
+                                        stream);
+    if (Ncap <= kRowThreads * 16)
+        return launch_row<16, kModeWhole>(logits, q_pos, n_comp, rows, rows, T, Ncap, m, k, 0, nullptr, idx_out,
+                                         cnt_out, stream);
+    if (Ncap <= kRowThreads * 32)
+        return launch_row<32, kModeWhole>(logits, q_pos, n_comp, rows, rows, T, Ncap, m, k, 0, nullptr, idx_out,
+                                         cnt_out, stream);
+    // Longer rows whose slices' candidates fit one CTA: two stages, the top k
+    // of every 32768-entry slice (one CTA a slice), then the top k of those
+    // candidates (one CTA a row). Exact: a key that its slice drops has k keys
+    // of the slice before it in (logit, lower index) order, so the row's top k
+    // does not hold it either.
+    if (const int S = row_slices(Ncap, k)) {
+        int32_t *cand = static_cast<int32_t *>(workspace);
+        cudaError_t e = launch_row<32, kModeSlice>(logits, q_pos, n_comp, rows, rows * S, T, Ncap, m, k, S, cand,
+                                                  nullptr, nullptr, stream);
+        if (e != cudaSuccess) return e;
+        if (S * k <= kRowThreads * 16)
+            return launch_row<16, kModeMerge>(logits, q_pos, n_comp, rows, rows, T, Ncap, m, k, S, cand, idx_out,
+                                             cnt_out, stream);
+        return launch_row<32, kModeMerge>(logits, q_pos, n_comp, rows, rows, T, Ncap, m, k, S, cand, idx_out, cnt_out,
+                                         stream);
+    }
     // Longer rows whose keys fit in the shared memory of a cluster (up to 8 x
     // 1024 threads x 44 keys): the 8-bit radix select, 256 threads a CTA up to
     // 65536 entries, 1024 above. Measured against the 11-bit cluster kernel

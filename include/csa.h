@@ -150,7 +150,10 @@ CSA_API csa_status_t csa_indexer_logits(const uint8_t *q_idx, const float *q_idx
  * ascending index order, the rest of the row set to -1; topk_cnt[b,t] = cnt.
  *   logits [B,T,Ncap] fp32 (entries >= n_vis are not read), topk_idx [B,T,k]
  *   int32, topk_cnt [B,T] int32. Requires 1 <= k <= min(Ncap, CSA_MAX_TOPK).
- * The workspace may be NULL when csa_workspace_bytes(CSA_OP_TOPK, ...) is 0. */
+ * The workspace may be NULL when csa_workspace_bytes(CSA_OP_TOPK, ...) is 0;
+ * rows of more than 32768 entries with ceil(Ncap / 32768) * k <= 32768 are
+ * selected in two stages and keep the slices' candidate indices there
+ * (4 * B * T * ceil(Ncap / 32768) * (k + 1) bytes). */
 CSA_API csa_status_t csa_topk(const float *logits, const int32_t *q_pos, const int32_t *n_comp,
                       int B, int T, int Ncap, int m, int k, int32_t *topk_idx, int32_t *topk_cnt,
                       void *workspace, size_t workspace_bytes, int32_t *status, cudaStream_t stream);

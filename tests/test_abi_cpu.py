@@ -51,6 +51,13 @@ def test_workspace_sizes(lib):
     assert step >= 4 * 32 * 32768 + 2 * 4 * 32 * 2048
     assert step % 256 == 0
     assert csd.csa_workspace_bytes(csd.OP_TOPK, 0, 1, 10, 1) == 0
+    # rows up to 32768 entries: one pass, no workspace; longer rows whose
+    # slices' candidates fit one pass: per (row, slice) k indices + k keys + its k-th key
+    assert csd.csa_workspace_bytes(csd.OP_TOPK, 32, 1, 32768, 2048) == 0
+    assert csd.csa_workspace_bytes(csd.OP_TOPK, 4, 4, 262144, 2048) == 4 * (16 * 8) * (2 * 2048 + 1)
+    assert csd.csa_workspace_bytes(csd.OP_TOPK, 3, 2, 70001, 1000) == 4 * (6 * 3) * (2 * 1000 + 1)
+    assert csd.csa_workspace_bytes(csd.OP_TOPK, 1, 1, 40000, 7) == 4 * (16 + 14 + 2)  # keys 16-byte aligned
+    assert csd.csa_workspace_bytes(csd.OP_TOPK, 1, 1, 17 * 32768, 2048) == 0  # 17 slices x 2048 > 32768
 
 
 def test_host_validation_rejects_before_launch(lib):
