@@ -125,6 +125,8 @@ def test_topk_heavy_ties_and_extremes(cuda_lib, ncap):
     vals[0, 0, 100:200] = 1e30
     vals[1, 1, :] = 0.0                       # all equal: lowest indices win
     vals[2, 0, ::7] = -np.float32(np.inf)
+    vals[0, 1, :] -= 4.0                      # few positive logits: K* negative for large k
+    vals[1, 0, :] = -np.abs(vals[1, 0, :]) - 1.0  # no positive logit
     lg = torch.tensor(vals, device="cuda")
     q_pos = torch.tensor([[4 * ncap, 4 * ncap + 1], [4 * ncap - 4, 4 * ncap - 1], [400, 401]], dtype=torch.int32,
                          device="cuda")
