@@ -114,10 +114,13 @@ def test_paged_cache_matches_contiguous_and_oracle(cuda_lib):
         assert np.array_equal(kv.cpu().numpy()[r][:okc[r]], okv[r][:okc[r]])
 
 
-# 5000, 8192 (8 keys a thread), 20001 (ragged rows: scalar loads) and 32768
-# (32 keys a thread): one CTA a row; 70001 (ragged) and 131076 (16-byte
-# loads): the 8-bit cluster select with 1024-thread CTAs
-@pytest.mark.parametrize("ncap", [5000, 8192, 20001, 32768, 70001, 131076])
+# One CTA a row: 5000, 8192 (8 keys a thread), 12289 (16, ragged rows:
+# scalar loads), 16384 (16), 20001 (32, ragged) and 32768 (32). Two stages
+# (32768-entry slices, then the candidates): 70001 and 131076 (merge of up to
+# 16384 candidates, indices staged in shared memory; with k = 7 the merge
+# rows are not a multiple of 4: scalar loads), 294913 (ten slices: 20480
+# candidates at k = 2048, the 32-key merge reading indices from memory).
+@pytest.mark.parametrize("ncap", [5000, 8192, 12289, 16384, 20001, 32768, 70001, 131076, 294913])
 def test_topk_heavy_ties_and_extremes(cuda_lib, ncap):
     rng = np.random.default_rng(0)
     B, T = 3, 2
