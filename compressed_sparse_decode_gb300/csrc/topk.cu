@@ -612,17 +612,21 @@ topk_radix8_kernel(const float *__restrict__ logits, const int32_t *__restrict__
 // [w * 32 * KPT, (w + 1) * 32 * KPT) of the row, loaded as coalesced 16-byte
 // groups: lane L holds the chunk's groups j * 32 + L (j < KPT / 4).
 //
-// The radix select takes two 16-bit digits, each counted into a 65536-bin
-// shared-memory histogram (two 16-bit counters a word: a row has at most 32768
-// keys): one predicated shared-memory add per key and pass, no per-key
-// branch. A descending scan over the histogram (thread t owns 64 bins, thread
-// order = descending bin order; one block scan of the per-thread totals) finds
-// the bin of the `need`-th largest counted key. The compaction gives every kept
-// key its slot in closed form, walking the row in index order (warp, group j,
-// lane, element): per group a warp scan of byte-packed kept counts, on top of
-// the kept counts of the warps before. Keys equal to K* are kept up to the
-// budget, lowest index first: when the budget cuts them (ties), the index of
-// the last one kept is found first, in the same index order.
+// The radix select takes two 16-bit digits. The first is counted into a
+// 65536-bin shared-memory histogram (two 16-bit counters a word: a row has at
+// most 32768 keys) with one predicated shared-memory add per key, no per-key
+// branch; a descending scan over it (thread t owns 64 bins, thread order =
+// descending bin order; one block scan of the per-thread totals, then the
+// owner's warp walks its 64 bins) finds the bin of the k-th largest key. The
+// keys of that bin, usually a few dozen, are listed and ranked against each
+// other by their low 16 bits (up to kRowMaxList of them; more are counted
+// into a second histogram the same way). The compaction builds a keep mask a
+// thread and gives every kept key its slot in closed form, in index order
+// (warp, group j, lane, element): per group a warp scan of byte-packed kept
+// counts, on top of the kept counts of the warps before, walking only the
+// set bits. Keys equal to K* are kept up to the budget, lowest index first:
+// when the budget cuts them (ties), the index of the last one kept is found
+// first, in the same index order.
 struct RowShared {
     int wsum[32];
     int wtot[32];
@@ -641,11 +645,6 @@ __device__ __forceinline__ void red_shared_add_if(uint32_t saddr, uint32_t v, bo
         "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q red.shared.add.u32 [%0], %1;\n\t}" ::"r"(saddr), "r"(v),
         "r"((uint32_t)c)
         : "memory");
-}
-__device__ __forceinline__ void st_global_if(int32_t *p, int32_t v, bool c) {
-    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q st.global.b32 [%0], %1;\n\t}" ::"l"(p), "r"(v),
-                 "r"((uint32_t)c)
-                 : "memory");
 }
 __device__ __forceinline__ uint32_t byte_sum(uint32_t x) { return (x & 0xFFu) + ((x >> 8) & 0xFFu) + ((x >> 16) & 0xFFu) + (x >> 24); }
 
